@@ -1,0 +1,216 @@
+"""Pins for the oracle's predictor: library layers, brute-force loops, invariants (CPU only)."""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from cem_search_transformer_gb300 import synthetic
+from oracle import predictor
+
+MICRO = synthetic.PredictorConfig("micro", layers=2, width=32, heads=4, mlp=64,
+                                  patch_tokens=5, embed_dim=12, precision="fp32")
+
+
+def _w(cfg, seed=0):
+    return predictor.prepare_weights(synthetic.make_weights(cfg, seed=seed, std=0.2), "fp32")
+
+
+def test_round_to_bf16_matches_torch():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(100000).astype(np.float32) * 10,
+                        np.array([0.0, -0.0, 1.0, 1.00390625, 1.005859375, 3.0e38, -1e-40],
+                                 np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(predictor.round_to_bf16(x), ref)
+
+
+def test_layer_norm_matches_torch():
+    rng = np.random.default_rng(1)
+    x, g, b = rng.standard_normal((7, 33)), rng.standard_normal(33), rng.standard_normal(33)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (33,), torch.from_numpy(g),
+                                         torch.from_numpy(b), eps=1e-5).numpy()
+    assert np.allclose(predictor.layer_norm(x, g, b, 1e-5), ref, rtol=1e-12, atol=1e-12)
+    y = predictor.layer_norm(x, np.ones(33), np.zeros(33), 0.0)
+    assert np.allclose(y.mean(-1), 0, atol=1e-12) and np.allclose(y.var(-1), 1, atol=1e-12)
+
+
+def test_gelu_matches_torch():
+    x = np.linspace(-8, 8, 2001)
+    ref = torch.nn.functional.gelu(torch.from_numpy(x)).numpy()
+    assert np.allclose(predictor.gelu(x), ref, rtol=1e-14, atol=1e-15)
+
+
+def test_block_causal_mask_brute_force():
+    T, nb = 3, 4
+    allowed = predictor.block_causal_allowed(nb, T)
+    for i in range(nb * T):
+        for j in range(nb * T):
+            assert allowed[i, j] == ((j // T) <= (i // T))
+
+
+def test_attention_brute_force_loops():
+    rng = np.random.default_rng(2)
+    heads, L, hd = 2, 7, 3
+    q, k, v = (rng.standard_normal((heads, L, hd)) for _ in range(3))
+    allowed = predictor.block_causal_allowed(3, 3)[:L, :L]
+    got = predictor.attention(q, k, v, allowed)
+    for h in range(heads):
+        for i in range(L):
+            scores = [sum(q[h, i, t] * k[h, j, t] for t in range(hd)) / math.sqrt(hd)
+                      if allowed[i, j] else None for j in range(L)]
+            m = max(s for s in scores if s is not None)
+            wts = [math.exp(s - m) if s is not None else 0.0 for s in scores]
+            z = sum(wts)
+            for t in range(hd):
+                want = sum(wts[j] * v[h, j, t] for j in range(L)) / z
+                assert abs(got[h, i, t] - want) < 1e-12
+
+
+def test_softmax_rows_sum_to_one():
+    rng = np.random.default_rng(3)
+    q, k = rng.standard_normal((2, 9, 4)) * 5, rng.standard_normal((2, 9, 4)) * 5
+    ones = np.ones((2, 9, 1))
+    allowed = predictor.block_causal_allowed(3, 3)
+    assert np.allclose(predictor.attention(q, k, ones, allowed), 1.0, atol=1e-13)
+
+
+def test_layer_matches_torch_encoder_layer():
+    """A pre-LN layer with the block-causal mask equals torch.nn.TransformerEncoderLayer."""
+    cfg = MICRO
+    w = _w(cfg, seed=4)
+    d, T, nb = cfg.width, cfg.tokens, 3
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((2, nb * T, d))
+    allowed = predictor.block_causal_allowed(nb, T)
+    got = predictor.transformer_layer(x, w, 1, cfg.heads, allowed, cfg.ln_eps)
+    layer = torch.nn.TransformerEncoderLayer(d, cfg.heads, cfg.mlp, dropout=0.0, activation="gelu",
+                                             layer_norm_eps=cfg.ln_eps, batch_first=True,
+                                             norm_first=True, dtype=torch.float64)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    with torch.no_grad():
+        layer.self_attn.in_proj_weight.copy_(t(w["l1.W_qkv"]))
+        layer.self_attn.in_proj_bias.copy_(t(w["l1.b_qkv"]))
+        layer.self_attn.out_proj.weight.copy_(t(w["l1.W_o"]))
+        layer.self_attn.out_proj.bias.copy_(t(w["l1.b_o"]))
+        layer.linear1.weight.copy_(t(w["l1.W_1"]))
+        layer.linear1.bias.copy_(t(w["l1.b_1"]))
+        layer.linear2.weight.copy_(t(w["l1.W_2"]))
+        layer.linear2.bias.copy_(t(w["l1.b_2"]))
+        layer.norm1.weight.copy_(t(w["l1.ln1_g"]))
+        layer.norm1.bias.copy_(t(w["l1.ln1_b"]))
+        layer.norm2.weight.copy_(t(w["l1.ln2_g"]))
+        layer.norm2.bias.copy_(t(w["l1.ln2_b"]))
+        ref = layer(t(x), src_mask=t(~allowed)).numpy()
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-11)
+
+
+def _incremental_rollout(w, cfg, z0, s0, actions):
+    """Independent KV-cached rollout: each layer attends over cached keys/values of earlier blocks."""
+    n, H, _ = actions.shape
+    d, hd, T = cfg.width, cfg.head_dim, cfg.tokens
+    cache = [[] for _ in range(cfg.layers)]
+    z, s, preds = np.broadcast_to(z0, (n,) + z0.shape), np.broadcast_to(s0, (n, len(s0))), []
+    for k in range(H):
+        x = predictor.embed_block(w, z, actions[:, k], s)
+        for l in range(cfg.layers):
+            h = predictor.layer_norm(x, w[f"l{l}.ln1_g"], w[f"l{l}.ln1_b"], cfg.ln_eps)
+            qkv = h @ w[f"l{l}.W_qkv"].T + w[f"l{l}.b_qkv"]
+            cache[l].append(qkv[..., d:])
+            kv = np.concatenate(cache[l], axis=1)
+            o = np.zeros((n, T, d))
+            for hh in range(cfg.heads):
+                qh = qkv[..., hh * hd:(hh + 1) * hd]
+                kh = kv[..., hh * hd:(hh + 1) * hd]
+                vh = kv[..., d + hh * hd:d + (hh + 1) * hd]
+                sc = qh @ kh.transpose(0, 2, 1) / math.sqrt(hd)
+                p = np.exp(sc - sc.max(-1, keepdims=True))
+                o[..., hh * hd:(hh + 1) * hd] = (p / p.sum(-1, keepdims=True)) @ vh
+            x = x + o @ w[f"l{l}.W_o"].T + w[f"l{l}.b_o"]
+            h2 = predictor.layer_norm(x, w[f"l{l}.ln2_g"], w[f"l{l}.ln2_b"], cfg.ln_eps)
+            x = x + predictor.gelu(h2 @ w[f"l{l}.W_1"].T + w[f"l{l}.b_1"]) @ w[f"l{l}.W_2"].T \
+                + w[f"l{l}.b_2"]
+        z = predictor.layer_norm(x[:, 2:], w["lnf_g"], w["lnf_b"], cfg.ln_eps) @ w["W_out"].T \
+            + w["b_out"]
+        preds.append(z)
+        s = s + actions[:, k]
+    return preds
+
+
+def test_rollout_equals_kv_cached_recurrence():
+    cfg = MICRO
+    w = _w(cfg, 6)
+    rng = np.random.default_rng(7)
+    z0, s0 = rng.standard_normal((cfg.patch_tokens, cfg.embed_dim)), rng.standard_normal(7)
+    acts = rng.uniform(-1, 1, (3, 3, 7))
+    full = predictor.rollout(w, cfg, z0, s0, acts)
+    inc = _incremental_rollout(w, cfg, z0, s0, acts)
+    for a, b in zip(full, inc):
+        assert np.allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_rollout_is_causal_in_actions():
+    """z_{k+1} depends on a_0..a_k only: changing the last action leaves earlier frames intact."""
+    cfg = MICRO
+    w = _w(cfg, 8)
+    rng = np.random.default_rng(9)
+    z0, s0 = rng.standard_normal((cfg.patch_tokens, cfg.embed_dim)), rng.standard_normal(7)
+    acts = rng.uniform(-1, 1, (2, 3, 7))
+    acts2 = acts.copy()
+    acts2[:, 2] += 0.3
+    p1, p2 = predictor.rollout(w, cfg, z0, s0, acts), predictor.rollout(w, cfg, z0, s0, acts2)
+    assert np.array_equal(p1[0], p2[0]) and np.array_equal(p1[1], p2[1])
+    assert not np.allclose(p1[2], p2[2])
+    # the state token carries a_0 into block 1: changing a_0 alters z_2 even with W_a = 0
+    w0 = dict(w, W_a=np.zeros_like(w["W_a"]))
+    acts3 = acts.copy()
+    acts3[:, 0] += 0.3
+    q1, q3 = predictor.rollout(w0, cfg, z0, s0, acts), predictor.rollout(w0, cfg, z0, s0, acts3)
+    assert np.array_equal(q1[0], q3[0]) and not np.allclose(q1[1], q3[1])
+
+
+def test_candidate_permutation_equivariance():
+    cfg = MICRO
+    w = _w(cfg, 10)
+    rng = np.random.default_rng(11)
+    z0, s0 = rng.standard_normal((cfg.patch_tokens, cfg.embed_dim)), rng.standard_normal(7)
+    acts = rng.uniform(-1, 1, (6, 2, 7))
+    perm = rng.permutation(6)
+    a = predictor.rollout(w, cfg, z0, s0, acts)[-1]
+    b = predictor.rollout(w, cfg, z0, s0, acts[perm])[-1]
+    assert np.allclose(a[perm], b, rtol=1e-13, atol=1e-14)
+
+
+def test_patch_permutation_equivariance_without_positions():
+    """With pos = 0 nothing but token content distinguishes patches: permuting the context
+    patches permutes the predicted patches (catches patch/token slicing mistakes)."""
+    cfg = MICRO
+    w = _w(cfg, 12)
+    w["pos"] = np.zeros_like(w["pos"])
+    rng = np.random.default_rng(13)
+    z0, s0 = rng.standard_normal((cfg.patch_tokens, cfg.embed_dim)), rng.standard_normal(7)
+    acts = rng.uniform(-1, 1, (2, 2, 7))
+    perm = rng.permutation(cfg.patch_tokens)
+    a = predictor.rollout(w, cfg, z0, s0, acts)
+    b = predictor.rollout(w, cfg, z0[perm], s0, acts)
+    for x, y in zip(a, b):
+        assert np.allclose(x[:, perm], y, rtol=1e-11, atol=1e-12)
+
+
+def test_actions_enter_only_through_action_and_state_tokens():
+    cfg = MICRO
+    w = _w(cfg, 14)
+    w["W_a"] = np.zeros_like(w["W_a"])
+    rng = np.random.default_rng(15)
+    z0, s0 = rng.standard_normal((cfg.patch_tokens, cfg.embed_dim)), rng.standard_normal(7)
+    acts = rng.uniform(-1, 1, (4, 1, 7))
+    z = predictor.rollout(w, cfg, z0, s0, acts)[0]
+    assert np.allclose(z, z[:1], rtol=0, atol=1e-14)
+
+
+def test_energy_closed_form():
+    rng = np.random.default_rng(16)
+    g = rng.standard_normal((5, 6))
+    z = np.stack([g + 0.25, g - 0.5, g])
+    assert np.allclose(predictor.energy_l1(z, g), [0.25, 0.5, 0.0], atol=1e-15)
