@@ -1,0 +1,215 @@
+"""Thin ctypes binding over libjepa.so (the C ABI in include/jepa_cem.h).
+
+Argument marshalling only: every step of the planning path runs in the library's CUDA
+kernels. torch is used for device memory and streams. There is no fallback: if the
+library is missing or fails to load, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import struct
+from typing import Dict, Optional
+
+import numpy as np
+
+from . import synthetic
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libjepa.so")
+_lib = None
+
+JEPA_OK = 0
+STATUS = {0: "ok", 1: "invalid argument", 2: "shape", 3: "not loaded", 4: "out of memory",
+          5: "CUDA error", 6: "timeout", 7: "unsupported"}
+EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string",
+           "jepa_weight_blob_bytes", "jepa_load_weights", "jepa_sample_actions", "jepa_philox4x32_10",
+           "jepa_predictor_forward", "jepa_cem_select_refit", "jepa_cem_plan",
+           "jepa_plan_kernel_count", "jepa_linear_bf16", "jepa_profile_enable",
+           "jepa_profile_read", "jepa_sync_check")
+
+
+class JepaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("layers", ctypes.c_int32), ("width", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("mlp", ctypes.c_int32), ("patch_tokens", ctypes.c_int32),
+                ("embed_dim", ctypes.c_int32), ("action_dim", ctypes.c_int32),
+                ("state_dim", ctypes.c_int32), ("max_horizon", ctypes.c_int32),
+                ("precision", ctypes.c_int32), ("ln_eps", ctypes.c_float),
+                ("max_chunk", ctypes.c_int32)]
+
+
+class Trace(ctypes.Structure):
+    _fields_ = [("mu", ctypes.c_void_p), ("sigma", ctypes.c_void_p), ("actions", ctypes.c_void_p),
+                ("energy", ctypes.c_void_p), ("elites", ctypes.c_void_p),
+                ("winner", ctypes.c_void_p)]
+
+
+def load(path: str = _LIB_PATH):
+    """Load the library (once) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (__graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    P, I, U64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
+    sig = {
+        "jepa_create": ([ctypes.POINTER(Config), I, ctypes.POINTER(P)], I),
+        "jepa_destroy": ([P], None),
+        "jepa_last_error": ([P], ctypes.c_char_p),
+        "jepa_status_string": ([I], ctypes.c_char_p),
+        "jepa_weight_blob_bytes": ([ctypes.POINTER(Config)], ctypes.c_size_t),
+        "jepa_load_weights": ([P, P, ctypes.c_size_t], I),
+        "jepa_sample_actions": ([P, P, P, I, I, I, I, U64, P, P], I),
+        "jepa_philox4x32_10": ([P, P, U64, I, P, P], I),
+        "jepa_predictor_forward": ([P, P, P, P, I, I, I, P, P, P, P], I),
+        "jepa_cem_select_refit": ([P, P, P, I, I, I, I, P, P, P, P], I),
+        "jepa_cem_plan": ([P, P, P, P, P, P, I, I, I, I, I, U64, P, ctypes.POINTER(Trace), P], I),
+        "jepa_plan_kernel_count": ([P, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64)], I),
+        "jepa_linear_bf16": ([P, P, P, P, I, I, I, I, P, P], I),
+        "jepa_profile_enable": ([P, I], I),
+        "jepa_profile_read": ([P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                               ctypes.POINTER(ctypes.c_int64)], I),
+        "jepa_sync_check": ([P, P], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def make_config(pc: synthetic.PredictorConfig, max_horizon: int = 1, max_chunk: int = 0) -> Config:
+    return Config(pc.layers, pc.width, pc.heads, pc.mlp, pc.patch_tokens, pc.embed_dim,
+                  pc.action_dim, pc.state_dim, max_horizon, 1 if pc.precision == "bf16" else 0,
+                  pc.ln_eps, max_chunk)
+
+
+def pack_weights(pc: synthetic.PredictorConfig, weights: Dict[str, np.ndarray]) -> bytes:
+    """Weight blob: 64-byte header + fp32 tensors in canonical order (format only)."""
+    hdr = struct.pack("<10i", 0x4150454A, 1, pc.layers, pc.width, pc.heads, pc.mlp,
+                      pc.patch_tokens, pc.embed_dim, pc.action_dim, pc.state_dim).ljust(64, b"\0")
+    shapes = synthetic.weight_shapes(pc)
+    parts = [hdr]
+    for name in synthetic.weight_names(pc):
+        w = np.ascontiguousarray(weights[name], dtype=np.float32)
+        assert w.shape == shapes[name], (name, w.shape)
+        parts.append(w.tobytes())
+    return b"".join(parts)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+class Planner:
+    """One library context (weights + workspaces + captured graphs) on one device."""
+
+    def __init__(self, pc: synthetic.PredictorConfig, max_horizon: int = 1, device: int = 0,
+                 max_chunk: int = 0):
+        self.lib = load()
+        self.pc = pc
+        self.cfg = make_config(pc, max_horizon, max_chunk)
+        h = ctypes.c_void_p()
+        st = self.lib.jepa_create(ctypes.byref(self.cfg), device, ctypes.byref(h))
+        if st != JEPA_OK:
+            raise JepaError(st, "jepa_create")
+        self.h = h
+
+    def _check(self, st: int, what: str):
+        if st != JEPA_OK:
+            raise JepaError(st, f"{what}: {self.lib.jepa_last_error(self.h).decode()}")
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.jepa_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def blob_bytes(self) -> int:
+        return self.lib.jepa_weight_blob_bytes(ctypes.byref(self.cfg))
+
+    def load_weights(self, weights: Dict[str, np.ndarray]):
+        blob = pack_weights(self.pc, weights)
+        buf = ctypes.create_string_buffer(blob, len(blob))
+        self._check(self.lib.jepa_load_weights(self.h, buf, len(blob)), "load_weights")
+
+    def load_blob(self, blob: bytes):
+        buf = ctypes.create_string_buffer(blob, len(blob))
+        return self.lib.jepa_load_weights(self.h, buf, len(blob))
+
+    def sample_actions(self, mu, sigma, B, N, H, rnd, seed, actions, stream=None):
+        self._check(self.lib.jepa_sample_actions(self.h, _ptr(mu), _ptr(sigma), B, N, H, rnd, seed,
+                                                 _ptr(actions), _stream(stream)), "sample_actions")
+
+    def philox(self, counters, seed, n, out, stream=None):
+        self._check(self.lib.jepa_philox4x32_10(self.h, _ptr(counters), seed, n, _ptr(out),
+                                                _stream(stream)), "philox4x32_10")
+
+    def predictor_forward(self, z_ctx, state0, actions, B, N, H, goal=None, z_pred=None,
+                          energy=None, stream=None):
+        self._check(self.lib.jepa_predictor_forward(
+            self.h, _ptr(z_ctx), _ptr(state0), _ptr(actions), B, N, H, _ptr(goal), _ptr(z_pred),
+            _ptr(energy), _stream(stream)), "predictor_forward")
+
+    def select_refit(self, energy, actions, B, N, H, K, mu_out, sigma_out, elites_out=None,
+                     stream=None):
+        self._check(self.lib.jepa_cem_select_refit(
+            self.h, _ptr(energy), _ptr(actions), B, N, H, K, _ptr(mu_out), _ptr(sigma_out),
+            _ptr(elites_out), _stream(stream)), "select_refit")
+
+    def plan(self, z0, state0, goal, mu0, sigma0, B, H, N, K, rounds, seed, action_out,
+             trace: Optional[Dict[str, object]] = None, stream=None):
+        """Inputs/outputs may be torch CUDA tensors, or raw host/device addresses (int)."""
+        tr = None
+        if trace is not None:
+            tr = Trace(*(_ptr(trace.get(k)) for k in ("mu", "sigma", "actions", "energy",
+                                                         "elites", "winner")))
+        self._check(self.lib.jepa_cem_plan(
+            self.h, _ptr(z0), _ptr(state0), _ptr(goal), _ptr(mu0), _ptr(sigma0), B, H, N, K,
+            rounds, seed, _ptr(action_out), ctypes.byref(tr) if tr is not None else None,
+            _stream(stream)), "cem_plan")
+
+    def kernel_count(self, B, H, N, K, rounds) -> int:
+        c = ctypes.c_int64()
+        self._check(self.lib.jepa_plan_kernel_count(self.h, B, H, N, K, rounds, ctypes.byref(c)),
+                    "plan_kernel_count")
+        return c.value
+
+    def linear_bf16(self, A, W, bias, M, N, K, gelu, out, stream=None):
+        self._check(self.lib.jepa_linear_bf16(self.h, _ptr(A), _ptr(W), _ptr(bias), M, N, K,
+                                              int(gelu), _ptr(out), _stream(stream)), "linear_bf16")
+
+    def profile_enable(self, on: bool):
+        self._check(self.lib.jepa_profile_enable(self.h, int(on)), "profile_enable")
+
+    def profile_read(self):
+        ms, fl, n = ctypes.c_double(), ctypes.c_double(), ctypes.c_int64()
+        self._check(self.lib.jepa_profile_read(self.h, ctypes.byref(ms), ctypes.byref(fl),
+                                               ctypes.byref(n)), "profile_read")
+        return ms.value, fl.value, n.value
+
+    def sync_check(self, stream=None):
+        self._check(self.lib.jepa_sync_check(self.h, _stream(stream)), "sync_check")

@@ -1,0 +1,382 @@
+// Tensor-core GEMM for the predictor's linear layers on sm_103a:
+//   out = epilogue(A[M,K] * W[N,K]^T), A and W bf16 (K-major), fp32 accumulation in TMEM.
+//
+// Design (GB300-first; the planning pages only say "bf16"):
+//   - persistent CTAs (one per SM) walk 128 x BN output tiles, m-major so the CTAs that run
+//     at the same time share A row blocks in L2 (W is at most a few MB and stays in L2);
+//   - warp 0: TMA producer (128B-swizzled 128x64 A and BNx64 W boxes into a STAGES-deep ring);
+//   - warp 1: TMEM allocator and single-thread tcgen05.mma issuer (M=128, N=BN, K=16 per
+//     instruction), committing to "smem empty" barriers and to a per-accumulator "full" barrier;
+//   - warps 2-5: epilogue; each reads its 32 TMEM lanes (rows) with tcgen05.ld 32x32b.x32,
+//     applies bias / GELU / residual / position / L1-energy (see common.cuh) and stores.
+//   - two TMEM accumulators (2 x BN columns) so the epilogue of tile i overlaps the MMAs of
+//     tile i+1.
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the kernel records an
+// error flag, stops issuing work, waits (bounded) for its own copies and MMAs, frees TMEM
+// and returns.
+#include "common.cuh"
+
+#include <cuda.h>
+
+namespace jepa {
+
+namespace {
+
+constexpr int BM = 128, BK = 64;
+constexpr int NUM_THREADS = 192;                 // 6 warps
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait. Returns false (after raising the abort flags) when the limit expires or
+// another role already aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_smem,
+                                       int* err_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_smem) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        *abort_smem = 1;
+        atomicExch(err_flag, 1);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
+// apart (stride byte offset), descriptor version 1 (bits 46-48), swizzle mode 2 (bits 61-63).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A bf16, B bf16, both K-major, N>>3, M>>4.
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int TMEM_COLS = 2 * BN;   // two accumulators; 256 or 512 (power of 2)
+  // ring + barriers (full, empty per stage; tfull, tempty per accumulator; teardown) + slot
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;  // +1024 alignment
+};
+
+}  // namespace
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              int M, int N, int K, Epilogue epi, int* err_flag) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+  const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + (2 * C::STAGES + 5) * 8);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_m = (M + BM - 1) / BM;
+  const int total = num_m * num_n;
+  const int num_k = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);   // one arrival per epilogue warp
+    }
+    mbar_init(teardown_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"((uint32_t)C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[8];
+      bool issued[8];
+      for (int s = 0; s < 8; ++s) issued[s] = false, issued_phase[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int m0 = (t / num_n) * BM, n0 = (t % num_n) * BN;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
+          tma_load_2d(sa, &tmA, kb * BK, m0, full_bar(stage));
+          tma_load_2d(sa + C::A_BYTES, &tmB, kb * BK, n0, full_bar(stage));
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == C::STAGES) stage = 0, phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded) until every copy this thread started has landed
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (!issued[s]) continue;
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(full_bar(s), issued_phase[s]) &&
+                 globaltimer() - t0 < WAIT_LIMIT_NS) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_bf16<BN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, err_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          const uint64_t adesc = desc_sw128(sa);
+          const uint64_t bdesc = desc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // advance 16 bf16 = 32 bytes along K inside the swizzle atom (+2 in 16-byte units)
+            mma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          }
+          mma_commit(empty_bar(stage));
+          if (++stage == C::STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        if (++acc == 2) acc = 0, acc_phase ^= 1u;
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      mma_commit(teardown_bar);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(teardown_bar, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;             // TMEM lanes quarter*32 .. +31
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err_flag)) break;
+      tc_fence_after();
+      const int m0 = (t / num_n) * BM, n_blk = t % num_n, n0 = n_blk * BN;
+      const int r = m0 + row_in_tile;
+      float esum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c), v);
+        if (r < M && n0 + c < N) esum += epilogue_run<32>(epi, r, n0 + c, v, min(32, N - n0 - c), N);
+      }
+      if (epi.mode == EPI_OUTPROJ && epi.goal && r < M)
+        epi.partial[(long long)r * epi.ntiles + n_blk] = esum;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) acc = 0, acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"((uint32_t)C::TMEM_COLS));
+  }
+}
+
+// ------------------------------- host side -------------------------------------------
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled get_encode() {
+  static PFN_encodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_encodeTiled)p;
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with a box of box_rows x 64.
+static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows) {
+  PFN_encodeTiled enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_tc_tile_n(int N) { return (N % 256 == 0 || N > 2048) ? 256 : 128; }
+
+template <int BN>
+static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
+                             int* err_flag, int num_sms, cudaStream_t s) {
+  using C = Cfg<BN>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, W, N, K, BN)) return cudaErrorInvalidValue;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  k_gemm_tc<BN><<<grid, NUM_THREADS, C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
+                         int* err_flag, int num_sms, cudaStream_t s) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  if (K <= 0 || K % 8 != 0 || (((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
+    return cudaErrorInvalidValue;
+  if (gemm_tc_tile_n(N) == 256) return launch_tc<256>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  return launch_tc<128>(A, W, M, N, K, epi, err_flag, num_sms, s);
+}
+
+}  // namespace jepa

@@ -1,0 +1,487 @@
+// Sampler, token assembly, LayerNorm, energy, elite selection / refit, and the fp32
+// (SIMT) GEMM and attention used by the fp32 precision mode.
+//
+// Method: "Real-time inference for JEPA world-model architectures with Ray", section
+// "Where the sixteen seconds actually goes" (draw candidates from a Gaussian, score
+// against the goal, keep the best K, re-centre the Gaussian).
+#include "common.cuh"
+
+#include <float.h>
+
+namespace jepa {
+
+// ---------------------------------------------------------------------------------
+// Candidate sampler: Philox4x32-10 (Salmon et al., SC'11) + Box-Muller.
+// Counter (n, b, round*Q + q, 0), key (seed lo, seed hi); word w of quad q feeds
+// element 4q + w of the candidate's H*A draws. Transform in fp64, stored as fp32.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
+    const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += W0;
+    k.y += W1;
+  }
+  return c;
+}
+
+__device__ __forceinline__ double uniform_open01(uint32_t x) {
+  return ((double)(x >> 9) + 0.5) * (1.0 / 8388608.0);
+}
+
+__global__ void k_sample(const float* __restrict__ mu, const float* __restrict__ sigma, int B,
+                         int N, int H, int A, int round, const uint64_t* __restrict__ seed_dev,
+                         uint64_t seed_val, float* __restrict__ actions) {
+  const int HA = H * A, Q = (HA + 3) / 4;
+  const long long total = (long long)B * N * Q;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int q = (int)(i % Q);
+  const long long bn = i / Q;
+  const int n = (int)(bn % N), b = (int)(bn / N);
+  const uint64_t seed = seed_dev ? *seed_dev : seed_val;
+  const uint4 w = philox4x32_10(make_uint4((uint32_t)n, (uint32_t)b, (uint32_t)(round * Q + q), 0u),
+                                make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+  double z[4];
+  {
+    const double r0 = sqrt(-2.0 * log(uniform_open01(w.x)));
+    double s, c;
+    sincospi(2.0 * uniform_open01(w.y), &s, &c);
+    z[0] = r0 * c;
+    z[1] = r0 * s;
+    const double r1 = sqrt(-2.0 * log(uniform_open01(w.z)));
+    sincospi(2.0 * uniform_open01(w.w), &s, &c);
+    z[2] = r1 * c;
+    z[3] = r1 * s;
+  }
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int e = 4 * q + t;
+    if (e < HA) {
+      const double m = (double)mu[(long long)b * HA + e];
+      const double sg = (double)sigma[(long long)b * HA + e];
+      double a = m + sg * z[t];
+      a = fmin(1.0, fmax(-1.0, a));
+      actions[bn * HA + e] = (float)a;
+    }
+  }
+}
+
+cudaError_t sample_actions(const float* mu, const float* sigma, int B, int N, int H, int A,
+                           int round, const uint64_t* seed_dev, uint64_t seed, float* actions,
+                           cudaStream_t s) {
+  const int Q = (H * A + 3) / 4;
+  const long long total = (long long)B * N * Q;
+  const int threads = 256;
+  k_sample<<<(unsigned)((total + threads - 1) / threads), threads, 0, s>>>(
+      mu, sigma, B, N, H, A, round, seed_dev, seed, actions);
+  return cudaGetLastError();
+}
+
+__global__ void k_philox_raw(const uint4* __restrict__ ctr, uint64_t seed, int n,
+                             uint4* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = philox4x32_10(ctr[i], make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+}
+
+cudaError_t philox_raw(const uint32_t* counters, uint64_t seed, int n, uint32_t* out,
+                       cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  k_philox_raw<<<(n + 255) / 256, 256, 0, s>>>(reinterpret_cast<const uint4*>(counters), seed, n,
+                                               reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// Token assembly for frame block k: [action a_k, state s_k, P patches].
+// s_k = state0[b] + sum_{j<k} a_j. Patch rows are copied from base (W_in z0 + b_in + pos,
+// computed once per problem) for k == 0; for k >= 1 the in-projection GEMM writes them.
+// ---------------------------------------------------------------------------------
+__global__ void k_assemble(const float* __restrict__ actions, const float* __restrict__ state0,
+                           const float* __restrict__ W_a, const float* __restrict__ b_a,
+                           const float* __restrict__ W_s, const float* __restrict__ b_s,
+                           const float* __restrict__ pos, const float* __restrict__ base,
+                           float* __restrict__ x, int cand0, int N, int H, int k, int A, int S,
+                           int P, int d) {
+  __shared__ float a_s[32], s_s[32];
+  const int lc = blockIdx.x;               // local candidate
+  const int cand = cand0 + lc;
+  const int b = cand / N;
+  const int T = P + 2;
+  const float* act = actions + (long long)cand * H * A;
+  if (threadIdx.x < A) a_s[threadIdx.x] = act[k * A + threadIdx.x];
+  if (threadIdx.x < S) {
+    float sv = state0[(long long)b * S + threadIdx.x];
+    for (int j = 0; j < k; ++j) sv += act[j * A + threadIdx.x];   // S == A (checked on the host)
+    s_s[threadIdx.x] = sv;
+  }
+  __syncthreads();
+  float* xr = x + (long long)lc * T * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float va = b_a[c] + pos[c], vs = b_s[c] + pos[d + c];
+    for (int j = 0; j < A; ++j) va += W_a[(long long)c * A + j] * a_s[j];
+    for (int j = 0; j < S; ++j) vs += W_s[(long long)c * S + j] * s_s[j];
+    xr[c] = va;
+    xr[d + c] = vs;
+  }
+  if (base) {
+    const float4* src = reinterpret_cast<const float4*>(base + (long long)b * P * d);
+    float4* dst = reinterpret_cast<float4*>(xr + 2 * (long long)d);
+    const int n4 = P * d / 4;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+  }
+}
+
+cudaError_t assemble_block(const float* actions, const float* state0, const float* W_a,
+                           const float* b_a, const float* W_s, const float* b_s, const float* pos,
+                           const float* base, float* x, int cand0, int ncand, int N, int H, int k,
+                           int A, int S, int P, int d, cudaStream_t s) {
+  if (ncand <= 0) return cudaSuccess;
+  k_assemble<<<ncand, 256, 0, s>>>(actions, state0, W_a, b_a, W_s, b_s, pos, base, x, cand0, N, H,
+                                   k, A, S, P, d);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// LayerNorm: one warp per row, fp32 statistics (two passes over registers).
+// ---------------------------------------------------------------------------------
+template <int VPL, bool OUT_BF16>
+__global__ void k_layernorm(const float* __restrict__ x, RowMap in_map, void* __restrict__ y,
+                            const float* __restrict__ g, const float* __restrict__ bta, int rows,
+                            int d, float eps) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const float* xr = x + map_row(in_map, warp) * d;
+  float v[VPL];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = lane + 32 * i;
+    v[i] = (c < d) ? xr[c] : 0.f;
+    s += v[i];
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s / d;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = lane + 32 * i;
+    const float t = (c < d) ? v[i] - mean : 0.f;
+    q += t * t;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  const float rstd = rsqrtf(q / d + eps);
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = lane + 32 * i;
+    if (c < d) {
+      const float t = (v[i] - mean) * rstd * g[c] + bta[c];
+      if (OUT_BF16)
+        reinterpret_cast<bf16*>(y)[(long long)warp * d + c] = __float2bfloat16_rn(t);
+      else
+        reinterpret_cast<float*>(y)[(long long)warp * d + c] = t;
+    }
+  }
+}
+
+template <int VPL>
+static cudaError_t launch_ln(const float* x, RowMap m, void* y, int y_bf16, const float* g,
+                             const float* b, int rows, int d, float eps, cudaStream_t s) {
+  const int threads = 256;
+  const unsigned blocks = (unsigned)(((long long)rows * 32 + threads - 1) / threads);
+  if (y_bf16)
+    k_layernorm<VPL, true><<<blocks, threads, 0, s>>>(x, m, y, g, b, rows, d, eps);
+  else
+    k_layernorm<VPL, false><<<blocks, threads, 0, s>>>(x, m, y, g, b, rows, d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t layernorm(const float* x, RowMap in_map, void* y, int y_bf16, const float* g,
+                      const float* b, int rows, int d, float eps, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (d <= 128) return launch_ln<4>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
+  if (d <= 512) return launch_ln<16>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
+  if (d <= 1024) return launch_ln<32>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
+  if (d <= 2048) return launch_ln<64>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
+  return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------------
+// Energy: E[c] = (1 / (P*E)) * sum over the candidate's P rows and ntiles partials.
+// One warp per candidate; lane-strided sums then a fixed xor tree (order independent of
+// how candidates are chunked).
+// ---------------------------------------------------------------------------------
+__global__ void k_energy_finalize(const float* __restrict__ partial, int P, int ntiles, int ncand,
+                                  float inv_count, float* __restrict__ energy) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= ncand) return;
+  const float* p = partial + (long long)warp * P * ntiles;
+  const int n = P * ntiles;
+  float s = 0.f;
+  for (int i = lane; i < n; i += 32) s += p[i];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) energy[warp] = s * inv_count;
+}
+
+cudaError_t energy_finalize(const float* partial, int P, int ntiles, int ncand, float inv_count,
+                            float* energy, cudaStream_t s) {
+  if (ncand <= 0) return cudaSuccess;
+  const int threads = 256;
+  k_energy_finalize<<<(ncand * 32 + threads - 1) / threads, threads, 0, s>>>(
+      partial, P, ntiles, ncand, inv_count, energy);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// Elite selection + refit: one CTA per problem. Keys (orderable energy bits << 32 | index)
+// are bitonic-sorted in shared memory, so ties go to the lower index and NaN sorts last.
+// Refit in fp64: mean and population std of the elites per (h, j).
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t orderable(float e) {
+  if (isnan(e)) return 0xFFFFFFFFu;
+  const uint32_t u = (e == 0.0f) ? 0u : __float_as_uint(e);   // -0 and +0 are the same energy
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void k_select_refit(const float* __restrict__ energy, const float* __restrict__ actions,
+                               int N, int HA, int K, int npow2, float* __restrict__ mu,
+                               float* __restrict__ sigma, int* __restrict__ elites,
+                               int* __restrict__ winner) {
+  extern __shared__ unsigned long long keys[];
+  const int b = blockIdx.x;
+  const float* e = energy + (long long)b * N;
+  for (int i = threadIdx.x; i < npow2; i += blockDim.x)
+    keys[i] = (i < N) ? (((unsigned long long)orderable(e[i]) << 32) | (unsigned)i)
+                      : 0xFFFFFFFFFFFFFFFFull;
+  __syncthreads();
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < npow2 / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = ((lo & size) == 0);
+        const unsigned long long a = keys[lo], c = keys[hi];
+        if ((a > c) == up) {
+          keys[lo] = c;
+          keys[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (elites)
+    for (int i = threadIdx.x; i < K; i += blockDim.x)
+      elites[(long long)b * K + i] = (int)(keys[i] & 0xFFFFFFFFu);
+  if (threadIdx.x == 0 && winner) winner[b] = (int)(keys[0] & 0xFFFFFFFFu);
+  // refit: one warp per (h, j) element
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const float* ab = actions + (long long)b * N * HA;
+  for (int el = warp; el < HA; el += nw) {
+    double s = 0.0;
+    for (int i = lane; i < K; i += 32) s += (double)ab[(long long)(keys[i] & 0xFFFFFFFFu) * HA + el];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const double m = s / K;
+    double q = 0.0;
+    for (int i = lane; i < K; i += 32) {
+      const double t = (double)ab[(long long)(keys[i] & 0xFFFFFFFFu) * HA + el] - m;
+      q += t * t;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    if (lane == 0) {
+      mu[(long long)b * HA + el] = (float)m;
+      sigma[(long long)b * HA + el] = (float)sqrt(q / K);
+    }
+  }
+}
+
+cudaError_t select_refit(const float* energy, const float* actions, int B, int N, int HA, int K,
+                         float* mu, float* sigma, int* elites, int* winner, cudaStream_t s) {
+  int npow2 = 1;
+  while (npow2 < N) npow2 <<= 1;
+  const size_t smem = (size_t)npow2 * sizeof(unsigned long long);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_select_refit, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_select_refit<<<B, 1024, smem, s>>>(energy, actions, N, HA, K, npow2, mu, sigma, elites, winner);
+  return cudaGetLastError();
+}
+
+__global__ void k_winner_action(const float* __restrict__ actions, const int* __restrict__ winner,
+                                int N, int HA, int A, float* __restrict__ out) {
+  const int b = blockIdx.x;
+  const int w = winner[b];
+  for (int j = threadIdx.x; j < A; j += blockDim.x)
+    out[(long long)b * A + j] = actions[((long long)b * N + w) * HA + j];
+}
+
+cudaError_t winner_action(const float* actions, const int* winner, int B, int N, int HA, int A,
+                          float* out, cudaStream_t s) {
+  k_winner_action<<<B, 32, 0, s>>>(actions, winner, N, HA, A, out);
+  return cudaGetLastError();
+}
+
+__global__ void k_set_u64(uint64_t* p, uint64_t v) { *p = v; }
+
+cudaError_t set_u64(uint64_t* p, uint64_t v, cudaStream_t s) {
+  k_set_u64<<<1, 1, 0, s>>>(p, v);
+  return cudaGetLastError();
+}
+
+__global__ void k_convert(const float* __restrict__ x, bf16* __restrict__ y, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    y[i] = __float2bfloat16_rn(x[i]);
+}
+
+cudaError_t convert_f32_bf16(const float* x, bf16* y, long long n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 65535LL * 16) blocks = 65535LL * 16;
+  k_convert<<<(unsigned)blocks, 256, 0, s>>>(x, y, n);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// fp32 SIMT GEMM (fp32 precision mode): C = A[M,K] * W[N,K]^T, 64x64 tiles, 4x4 per thread.
+// The energy partial of a row is the fixed-order sum over the tile's 64 columns.
+// ---------------------------------------------------------------------------------
+constexpr int SG_BM = 64, SG_BN = 64, SG_BK = 16;
+
+__global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ A,
+                                                   const float* __restrict__ W, int M, int N,
+                                                   int K, Epilogue epi) {
+  __shared__ float As[SG_BK][SG_BM + 4];
+  __shared__ float Ws[SG_BK][SG_BN + 4];
+  __shared__ float red[SG_BM][17];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * SG_BM, n0 = blockIdx.x * SG_BN;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += SG_BK) {
+    for (int i = threadIdx.x; i < SG_BM * SG_BK; i += 256) {
+      const int r = i / SG_BK, kk = i % SG_BK;
+      const int gr = m0 + r, gk = k0 + kk;
+      As[kk][r] = (gr < M && gk < K) ? A[(long long)gr * K + gk] : 0.f;
+      const int gn = n0 + r;
+      Ws[kk][r] = (gn < N && gk < K) ? W[(long long)gn * K + gk] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < SG_BK; ++kk) {
+      float a[4], w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = Ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  const int c = n0 + tx * 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = m0 + ty * 4 + i;
+    float s = 0.f;
+    if (r < M && c < N) s = epilogue_run<4>(epi, r, c, acc[i], min(4, N - c), N);
+    red[ty * 4 + i][tx] = s;
+  }
+  if (epi.mode == EPI_OUTPROJ && epi.goal) {
+    __syncthreads();
+    if (threadIdx.x < SG_BM) {
+      const int r = m0 + threadIdx.x;
+      float s = 0.f;
+      for (int j = 0; j < 16; ++j) s += red[threadIdx.x][j];
+      if (r < M) epi.partial[(long long)r * epi.ntiles + blockIdx.x] = s;
+    }
+  }
+}
+
+int gemm_simt_tile_n() { return SG_BN; }
+
+cudaError_t gemm_simt_f32(const float* A, const float* W, int M, int N, int K, const Epilogue& epi,
+                          cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  dim3 grid((N + SG_BN - 1) / SG_BN, (M + SG_BM - 1) / SG_BM);
+  k_gemm_simt<<<grid, 256, 0, s>>>(A, W, M, N, K, epi);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// fp32 attention (fp32 mode): one warp per query row; scores in shared memory,
+// max-subtracted softmax, then P*V with each lane owning head_dim/32 output columns.
+// ---------------------------------------------------------------------------------
+constexpr int FA32_WARPS = 8;
+
+__global__ void __launch_bounds__(FA32_WARPS * 32) k_attention_f32(
+    const float* __restrict__ q, const float* __restrict__ kv, float* __restrict__ o, int T, int Lk,
+    long long kv_stride, int heads, int d, float scale) {
+  extern __shared__ float sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * FA32_WARPS + warp;
+  const int h = blockIdx.y, cand = blockIdx.z;
+  const int hd = d / heads;
+  if (t >= T) return;
+  float* sc = sm + warp * Lk;
+  const float* qr = q + ((long long)cand * T + t) * d + h * hd;
+  const float* kb = kv + (long long)cand * kv_stride * 2 * d + h * hd;
+  const float* vb = kb + d;
+  float mx = -FLT_MAX;
+  for (int j = lane; j < Lk; j += 32) {
+    const float* kr = kb + (long long)j * 2 * d;
+    float s = 0.f;
+    for (int c = 0; c < hd; ++c) s = fmaf(qr[c], kr[c], s);
+    s *= scale;
+    sc[j] = s;
+    mx = fmaxf(mx, s);
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float sum = 0.f;
+  for (int j = lane; j < Lk; j += 32) {
+    const float p = expf(sc[j] - mx);
+    sc[j] = p;
+    sum += p;
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  __syncwarp();
+  const float inv = 1.f / sum;
+  for (int c = lane; c < hd; c += 32) {
+    float acc = 0.f;
+    for (int j = 0; j < Lk; ++j) acc = fmaf(sc[j], vb[(long long)j * 2 * d + c], acc);
+    o[((long long)cand * T + t) * d + h * hd + c] = acc * inv;
+  }
+}
+
+cudaError_t attention_f32(const float* q, const float* kv, float* o, int ncand, int T, int Lk,
+                          long long kv_cand_stride_rows, int heads, int d, cudaStream_t s) {
+  if (ncand <= 0) return cudaSuccess;
+  const size_t smem = (size_t)FA32_WARPS * Lk * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_attention_f32,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid((T + FA32_WARPS - 1) / FA32_WARPS, heads, ncand);
+  const float scale = 1.0f / sqrtf((float)(d / heads));
+  k_attention_f32<<<grid, FA32_WARPS * 32, smem, s>>>(q, kv, o, T, Lk, kv_cand_stride_rows, heads, d,
+                                                       scale);
+  return cudaGetLastError();
+}
+
+}  // namespace jepa

@@ -1,0 +1,192 @@
+/*
+ * jepa_cem.h -- C ABI of the GB300 (sm_103a) CEM planner over an action-conditioned
+ * JEPA world-model predictor.
+ *
+ * What it computes follows "Real-time inference for JEPA world-model architectures
+ * with Ray", section "Where the sixteen seconds actually goes": one planning step
+ * draws N candidate action sequences from a Gaussian, pushes each through the
+ * predictor, scores the prediction against the goal embedding, keeps the best K,
+ * re-centres the Gaussian on them, repeats for R rounds and returns only the first
+ * action of the winning sequence. Section "Measured on 8x A100" adds that the
+ * predictor is frame-causal (so a KV cache across rollout steps is exact), that it
+ * runs in bf16 with flash attention, and that the same seed gives the same plan
+ * however the candidates are batched.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, row-major, float32 unless stated. Shapes use
+ *     B problems, N candidates, H horizon steps, A action dim, S state dim,
+ *     P patch tokens per frame, E embedding dim.
+ *   - Pointers marked "dev" are device pointers on the context's device. Pointers
+ *     marked "dev|host" may be device memory or host memory (pinned or pageable);
+ *     the library copies them with cudaMemcpyAsync(cudaMemcpyDefault).
+ *   - The caller owns every buffer it passes; the context owns weights, workspaces
+ *     and captured CUDA graphs. Nothing passed in is retained after the call returns
+ *     except through the stream's pending work.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is enqueued
+ *     asynchronously; outputs are valid once the stream has been synchronised.
+ *   - Every call returns a jepa_status and never aborts the process. After an error
+ *     the output contents are unspecified; the context stays usable and
+ *     jepa_last_error() describes the failure. A context must not be used from two
+ *     host threads at once.
+ */
+#ifndef JEPA_CEM_H_
+#define JEPA_CEM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  JEPA_OK = 0,
+  JEPA_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, K > N, ... */
+  JEPA_ERR_SHAPE = 2,        /* shape outside what the context was created for */
+  JEPA_ERR_NOT_LOADED = 3,   /* weights not loaded yet */
+  JEPA_ERR_OOM = 4,          /* device allocation failed */
+  JEPA_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+  JEPA_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up (kernel returned early) */
+  JEPA_ERR_UNSUPPORTED = 7   /* device is not sm_103 / feature not built */
+} jepa_status;
+
+typedef enum { JEPA_FP32 = 0, JEPA_BF16 = 1 } jepa_precision;
+
+/* Predictor shape. Pre-LN transformer, block-causal over frame blocks of
+ * T = patch_tokens + 2 tokens ([action, state, P patches]). */
+typedef struct {
+  int32_t layers;        /* L */
+  int32_t width;         /* d, multiple of 32 (bf16: multiple of 64) */
+  int32_t heads;         /* h; head dim d/h = 64 in bf16 mode, <= 128 in fp32 mode */
+  int32_t mlp;           /* m, hidden width of the GELU MLP */
+  int32_t patch_tokens;  /* P */
+  int32_t embed_dim;     /* E, multiple of 32 (bf16: multiple of 64) */
+  int32_t action_dim;    /* A (7 in the planning workloads) */
+  int32_t state_dim;     /* S (7) */
+  int32_t max_horizon;   /* largest H any call will use; sizes the KV cache */
+  int32_t precision;     /* jepa_precision: FP32 = SIMT fp32 path, BF16 = tensor-core path */
+  float ln_eps;          /* LayerNorm epsilon (1e-5) */
+  int32_t max_chunk;     /* candidates per predictor pass (0 = library default); bounds workspace */
+} jepa_config;
+
+typedef struct jepa_ctx jepa_ctx;
+
+/* Optional per-round record of a plan. All device pointers; each may be NULL. */
+typedef struct {
+  float* mu;        /* [R+1, B, H, A]  mu_0 .. mu_R */
+  float* sigma;     /* [R+1, B, H, A]  sigma_0 .. sigma_R */
+  float* actions;   /* [R, B, N, H, A] clipped candidates of each round */
+  float* energy;    /* [R, B, N]       energies of each round */
+  int32_t* elites;  /* [R, B, K]       elite indices, ascending (energy, index) */
+  int32_t* winner;  /* [B]             winner of the final round */
+} jepa_cem_trace;
+
+/* Create a context on CUDA device `device` for predictor shape *cfg.
+ * Fails with JEPA_ERR_UNSUPPORTED unless the device is compute capability 10.3. */
+jepa_status jepa_create(const jepa_config* cfg, int device, jepa_ctx** out);
+
+/* Free the context and everything it owns. Synchronises the device first. NULL is a no-op. */
+void jepa_destroy(jepa_ctx* ctx);
+
+/* Text of the last error on this context ("" if none). Valid until the next call on ctx. */
+const char* jepa_last_error(const jepa_ctx* ctx);
+
+/* Static name of a status code. */
+const char* jepa_status_string(jepa_status s);
+
+/* Size in bytes of the weight blob for *cfg: a 64-byte header (int32 magic 0x4150454A,
+ * version 1, layers, width, heads, mlp, patch_tokens, embed_dim, action_dim, state_dim,
+ * then zeros) followed by float32 tensors in this order, each row-major [out, in]:
+ * W_in[d,E] b_in[d] W_a[d,A] b_a[d] W_s[d,S] b_s[d] pos[T,d], per layer
+ * {ln1_g[d] ln1_b[d] W_qkv[3d,d] b_qkv[3d] W_o[d,d] b_o[d] ln2_g[d] ln2_b[d]
+ *  W_1[m,d] b_1[m] W_2[d,m] b_2[d]}, lnf_g[d] lnf_b[d] W_out[E,d] b_out[E]. */
+size_t jepa_weight_blob_bytes(const jepa_config* cfg);
+
+/* Upload predictor weights from a host blob (format above). Validates the header
+ * against the context's config (JEPA_ERR_SHAPE on mismatch), converts the GEMM
+ * matrices to bf16 in bf16 mode, and blocks until the upload is done. On error the
+ * previously loaded weights (if any) stay in place. */
+jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes);
+
+/* Candidate sampler (planning page: "draws 800 candidate action sequences from a
+ * Gaussian centered on its current best guess").
+ *   mu, sigma [B,H,A] dev; actions [B,N,H,A] dev (output).
+ * eps[b,n,h,j] comes from Philox4x32-10 with key (seed lo, seed hi) and counter
+ * (n, b, round*Q + q, 0), Q = ceil(H*A/4), q = (h*A+j)/4, word (h*A+j)%4, turned into
+ * normals by Box-Muller on u = ((x>>9)+0.5)*2^-23 (cos for words 0/2, sin for 1/3);
+ * actions = clip(mu + sigma*eps, -1, 1). Draws depend only on (seed, b, n, round, h, j). */
+jepa_status jepa_sample_actions(jepa_ctx* ctx, const float* mu, const float* sigma, int B, int N,
+                                int H, int round, uint64_t seed, float* actions, void* stream);
+
+/* The sampler's generator alone: out[i] = Philox4x32-10(counter[i], key = (seed lo, seed hi)),
+ * the four 32-bit output words of counter words counters[4i .. 4i+3] (uint32, dev; n >= 1).
+ * Exposed so that integer outputs can be compared bit for bit. */
+jepa_status jepa_philox4x32_10(jepa_ctx* ctx, const uint32_t* counters, uint64_t seed, int n,
+                               uint32_t* out, void* stream);
+
+/* Predictor rollout and L1 energy (the "push every one through the predictor, score
+ * the results against the goal embedding" step; frame-causal with a KV cache).
+ *   z_ctx [B,P,E] dev   encoded context frame of each problem
+ *   state0 [B,S] dev    state of each problem (s_k = s_{k-1} + a_{k-1})
+ *   actions [B,N,H,A] dev
+ *   goal [B,P,E] dev or NULL
+ *   z_pred [B,N,P,E] dev or NULL   output: the last predicted frame z_H
+ *   energy [B,N] dev or NULL       output: mean |z_H - goal| (needs goal)
+ * 1 <= H <= cfg.max_horizon. */
+jepa_status jepa_predictor_forward(jepa_ctx* ctx, const float* z_ctx, const float* state0,
+                                   const float* actions, int B, int N, int H, const float* goal,
+                                   float* z_pred, float* energy, void* stream);
+
+/* Elite selection and Gaussian refit ("keeps the best 80, and re-centers the Gaussian on
+ * them"): per problem, the K lowest energies ordered by (energy, index), NaN last; then
+ * mu' = elite mean and sigma' = elite population std per (h, j).
+ *   energy [B,N] dev; actions [B,N,H,A] dev; mu_out, sigma_out [B,H,A] dev (outputs);
+ *   elites_out [B,K] int32 dev or NULL. 1 <= K <= N <= 8192. */
+jepa_status jepa_cem_select_refit(jepa_ctx* ctx, const float* energy, const float* actions, int B,
+                                  int N, int H, int K, float* mu_out, float* sigma_out,
+                                  int32_t* elites_out, void* stream);
+
+/* One full planning step: R rounds of sample -> predictor -> energy -> select/refit with
+ * no host round-trip between rounds (one captured CUDA graph per (B,H,N,K,R), cached in
+ * the context), then action_out[b] = first action of problem b's lowest-energy
+ * candidate in the final round.
+ *   z0, goal [B,P,E], state0 [B,S], mu0, sigma0 [B,H,A]: dev|host inputs
+ *   action_out [B,A]: dev|host output
+ *   trace: NULL or per-round record (device pointers, see jepa_cem_trace)
+ * The first call for a new (B,H,N,K,R) allocates workspace and captures the graph. */
+jepa_status jepa_cem_plan(jepa_ctx* ctx, const float* z0, const float* state0, const float* goal,
+                          const float* mu0, const float* sigma0, int B, int H, int N, int K,
+                          int rounds, uint64_t seed, float* action_out,
+                          const jepa_cem_trace* trace, void* stream);
+
+/* Number of kernel launches one jepa_cem_plan call with these sizes makes (captures
+ * the graph if needed). */
+jepa_status jepa_plan_kernel_count(jepa_ctx* ctx, int B, int H, int N, int K, int rounds,
+                                   int64_t* count);
+
+/* Dense linear layer on the tensor-core GEMM used by the predictor (bf16 in, fp32
+ * accumulate): out[M,N] = act(A[M,K] * W[N,K]^T + bias[N]).
+ *   A, W: bf16 bit patterns (uint16) dev; bias [N] dev or NULL; out [M,N] float32 dev.
+ *   gelu: 0 = identity, 1 = erf GELU. K a multiple of 8. Needs a bf16 context. */
+jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W,
+                             const float* bias, int M, int N, int K, int gelu, float* out,
+                             void* stream);
+
+/* Kernel-level timing of the predictor GEMMs inside plan graphs. enable != 0 makes graphs
+ * captured afterwards record a CUDA event pair around every GEMM launch (graphs captured
+ * before keep their state). jepa_profile_read (after the stream is synchronised) returns
+ * the summed event time, summed algorithmic FLOPs (2*M*N*K) and launch count of the
+ * GEMMs in the most recent plan call, and resets nothing. */
+jepa_status jepa_profile_enable(jepa_ctx* ctx, int enable);
+jepa_status jepa_profile_read(jepa_ctx* ctx, double* gemm_ms, double* gemm_flops,
+                              int64_t* gemm_launches);
+
+/* Synchronise `stream`, then report JEPA_ERR_TIMEOUT if a bounded device-side wait in
+ * any kernel of this context gave up since the last check (the flag is then cleared). */
+jepa_status jepa_sync_check(jepa_ctx* ctx, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JEPA_CEM_H_ */

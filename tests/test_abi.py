@@ -1,0 +1,65 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares (CPU only:
+no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from cem_search_transformer_gb300 import binding, build_lib, synthetic
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    syms = set()
+    for name in os.listdir(os.path.join(ROOT, "include")):
+        if name.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", name)).read()
+            syms |= set(re.findall(r"\b(jepa_[a-z0-9_]+)\s*\(", text))
+    return syms
+
+
+@pytest.fixture(scope="module")
+def cdll():
+    path = build_lib.build()
+    return ctypes.CDLL(path)
+
+
+def test_every_declared_symbol_is_exported(cdll):
+    declared = _declared_symbols()
+    assert len(declared) >= 15
+    for s in sorted(declared):
+        assert hasattr(cdll, s), s
+    assert declared == set(binding.EXPORTS)
+
+
+def test_blob_size_matches_packer(cdll):
+    lib = binding.load(build_lib.LIB)
+    for pc, H in ((synthetic.TINY, 1), (synthetic.SMALL, 2)):
+        cfg = binding.make_config(pc, H)
+        weights = synthetic.make_weights(pc)
+        assert lib.jepa_weight_blob_bytes(ctypes.byref(cfg)) == len(binding.pack_weights(pc, weights))
+
+
+def test_invalid_configs_rejected_without_gpu(cdll):
+    lib = binding.load(build_lib.LIB)
+    bad = binding.make_config(synthetic.TINY, 1)
+    bad.heads = 3                       # width not divisible by heads
+    assert lib.jepa_weight_blob_bytes(ctypes.byref(bad)) == 0
+    bf = binding.make_config(synthetic.SMALL, 1)
+    bf.heads = 12                       # bf16 path needs head dim 64
+    assert lib.jepa_weight_blob_bytes(ctypes.byref(bf)) == 0
+    h = ctypes.c_void_p()
+    assert lib.jepa_create(ctypes.byref(bad), 0, ctypes.byref(h)) == 2   # JEPA_ERR_SHAPE
+    assert lib.jepa_status_string(6) == b"device wait timed out"
+    assert lib.jepa_last_error(None) == b""
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "cem_search_transformer_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f

@@ -1,0 +1,170 @@
+"""The whole planning step (sample -> predictor -> energy -> select/refit, R rounds in one
+captured graph, first action of the winner) against the oracle, round by round
+(teacher-forced on the GPU's own mu_r, sigma_r so one divergent elite cannot cascade) and
+end to end where the energy gaps make the answer unique."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from cem_search_transformer_gb300 import synthetic
+from gpu_helpers import (TOL_BF16_ENERGY_REL, TOL_EPS, TOL_FP32_REL, TOL_REFIT, cuda,
+                         energy_gap_allows, host, make_planner, oracle_weights_for, rel_err)
+from oracle import cem, philox, predictor
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan(p, pc, wl, z0, goal, s0, mu0, sg0):
+    B, N, K, R, H = z0.shape[0], wl.N, wl.K, wl.rounds, wl.horizon
+    out = torch.zeros(B, 7, device="cuda")
+    tr = {"mu": torch.zeros(R + 1, B, H, 7, device="cuda"),
+          "sigma": torch.zeros(R + 1, B, H, 7, device="cuda"),
+          "actions": torch.zeros(R, B, N, H, 7, device="cuda"),
+          "energy": torch.zeros(R, B, N, device="cuda"),
+          "elites": torch.zeros(R, B, K, dtype=torch.int32, device="cuda"),
+          "winner": torch.zeros(B, dtype=torch.int32, device="cuda")}
+    p.plan(cuda(z0), cuda(s0), cuda(goal), cuda(mu0), cuda(sg0), B, H, N, K, R, wl.seed, out, trace=tr)
+    p.sync_check()
+    return host(out), {k: host(v) for k, v in tr.items()}
+
+
+def _teacher_forced(name, pc, wl, z0, goal, s0, tr, b, energy_tol, sample=None):
+    """Per round: sampler, energies (all or a sample), elites and refit vs the oracle."""
+    N, K, H = wl.N, wl.K, wl.horizon
+    w = oracle_weights_for(name)
+    gap_rounds = 0
+    for r in range(wl.rounds):
+        a_gpu = tr["actions"][r, b]
+        a_ref = philox.sample_actions(tr["mu"][r, b], tr["sigma"][r, b],
+                                      philox.sample_eps(wl.seed, b, r, N, H, 7))
+        assert np.max(np.abs(a_gpu - a_ref)) < TOL_EPS
+        idx = np.arange(N) if sample is None else np.array(sample)
+        z = predictor.rollout(w, pc, z0[b], s0[b], a_gpu[idx].astype(np.float64))[-1]
+        e_ref = predictor.energy_l1(z, goal[b])
+        assert rel_err(tr["energy"][r, b][idx], e_ref) < energy_tol
+        if sample is None and energy_gap_allows(e_ref, K, energy_tol):
+            gap_rounds += 1
+            assert set(cem.select_elites(e_ref, K)) == set(tr["elites"][r, b])
+        el = cem.select_elites(tr["energy"][r, b], K)
+        assert np.array_equal(el, tr["elites"][r, b])
+        m_ref, s_ref = cem.refit(a_gpu[el])
+        assert np.max(np.abs(tr["mu"][r + 1, b] - m_ref)) < TOL_REFIT
+        assert np.max(np.abs(tr["sigma"][r + 1, b] - s_ref)) < TOL_REFIT
+    assert tr["winner"][b] == tr["elites"][-1, b][0]
+    return gap_rounds
+
+
+def test_tiny_fp32_plan_matches_oracle():
+    wl = synthetic.WORKLOADS["tiny"]
+    pc = wl.predictor
+    p = make_planner("tiny", max_horizon=wl.horizon)
+    z0, goal, s0 = synthetic.make_problems(pc, 1)
+    mu0, sg0 = synthetic.make_gaussian(pc, 1, wl.horizon)
+    out, tr = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    gaps = _teacher_forced("tiny", pc, wl, z0, goal, s0, tr, 0, TOL_FP32_REL)
+    assert np.array_equal(out[0], tr["actions"][-1, 0][tr["winner"][0], 0])
+    ref = cem.plan(synthetic.make_weights(pc), pc, z0[0], s0[0], goal[0], mu0[0], sg0[0], wl.N,
+                   wl.K, wl.rounds, wl.seed)
+    if gaps == wl.rounds:
+        assert np.max(np.abs(out[0] - ref["action"])) < 1e-4
+    print(f"tiny: {gaps}/{wl.rounds} rounds with a decisive elite gap; "
+          f"action |diff| {np.max(np.abs(out[0] - ref['action'])):.2e}")
+    p.close()
+
+
+def test_small_bf16_plan_teacher_forced():
+    wl = synthetic.WORKLOADS["small"]
+    pc = wl.predictor
+    p = make_planner("small", max_horizon=wl.horizon)
+    z0, goal, s0 = synthetic.make_problems(pc, 1)
+    mu0, sg0 = synthetic.make_gaussian(pc, 1, wl.horizon)
+    out, tr = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    _teacher_forced("small", pc, wl, z0, goal, s0, tr, 0, TOL_BF16_ENERGY_REL, sample=range(0, 200, 19))
+    assert np.array_equal(out[0], tr["actions"][-1, 0][tr["winner"][0], 0])
+    p.close()
+
+
+def test_full_shape_plan_teacher_forced():
+    """The benchmark workload itself (N=800, K=80, R=10, full-shape predictor)."""
+    wl = synthetic.WORKLOADS["full"]
+    pc = wl.predictor
+    p = make_planner("full", max_horizon=1)
+    z0, goal, s0 = synthetic.make_problems(pc, 1)
+    mu0, sg0 = synthetic.make_gaussian(pc, 1, 1)
+    out, tr = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    w = oracle_weights_for("full")
+    for r in range(wl.rounds):
+        a_ref = philox.sample_actions(tr["mu"][r, 0], tr["sigma"][r, 0],
+                                      philox.sample_eps(wl.seed, 0, r, wl.N, 1, 7))
+        assert np.max(np.abs(tr["actions"][r, 0] - a_ref)) < TOL_EPS
+        el = cem.select_elites(tr["energy"][r, 0], wl.K)
+        assert np.array_equal(el, tr["elites"][r, 0])
+        m_ref, s_ref = cem.refit(tr["actions"][r, 0][el])
+        assert np.max(np.abs(tr["mu"][r + 1, 0] - m_ref)) < TOL_REFIT
+        assert np.max(np.abs(tr["sigma"][r + 1, 0] - s_ref)) < TOL_REFIT
+    for r, idx in ((0, [int(tr["elites"][0, 0][0]), 5]), (wl.rounds - 1, [int(tr["winner"][0])])):
+        z = predictor.rollout(w, pc, z0[0], s0[0], tr["actions"][r, 0][idx].astype(np.float64))[-1]
+        assert rel_err(tr["energy"][r, 0][idx], predictor.energy_l1(z, goal[0])) < TOL_BF16_ENERGY_REL
+    assert np.array_equal(out[0], tr["actions"][-1, 0][tr["winner"][0], 0])
+    p.close()
+
+
+def test_plan_batching_and_host_buffers():
+    """B problems planned together equal each planned alone (bitwise), and host buffers give
+    the same answer as device buffers."""
+    wl = synthetic.WORKLOADS["small"]
+    pc = wl.predictor
+    p = make_planner("small", max_horizon=2)
+    B = 3
+    z0, goal, s0 = synthetic.make_problems(pc, B)
+    mu0, sg0 = synthetic.make_gaussian(pc, B, 2)
+    N, K, R = 64, 8, 3
+    out = torch.zeros(B, 7, device="cuda")
+    p.plan(cuda(z0), cuda(s0), cuda(goal), cuda(mu0), cuda(sg0), B, 2, N, K, R, 9, out)
+    p.sync_check()
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hz, hs, hg, hm, hsg = pin(z0), pin(s0), pin(goal), pin(mu0), pin(sg0)
+    hout = torch.zeros(B, 7).pin_memory()
+    p.plan(hz.data_ptr(), hs.data_ptr(), hg.data_ptr(), hm.data_ptr(), hsg.data_ptr(), B, 2, N, K,
+           R, 9, hout.data_ptr())
+    p.sync_check()
+    assert np.array_equal(hout.numpy(), host(out))
+    # a batch with problem 0 replaced keeps problems 1..B-1 bitwise
+    z0b = z0.copy()
+    z0b[0] = synthetic.make_problems(pc, 1, seed_base=77)[0][0]
+    out2 = torch.zeros(B, 7, device="cuda")
+    p.plan(cuda(z0b), cuda(s0), cuda(goal), cuda(mu0), cuda(sg0), B, 2, N, K, R, 9, out2)
+    p.sync_check()
+    assert np.array_equal(host(out2)[1:], host(out)[1:])
+    p.close()
+
+
+def test_plan_errors_and_kernel_count():
+    from cem_search_transformer_gb300 import binding
+    from cem_search_transformer_gb300.binding import JepaError
+    pc = synthetic.TINY
+    p = binding.Planner(pc, max_horizon=1)
+    z = torch.zeros(1, 16, 64, device="cuda")
+    s = torch.zeros(1, 7, device="cuda")
+    m = torch.zeros(1, 1, 7, device="cuda")
+    o = torch.zeros(1, 7, device="cuda")
+    with pytest.raises(JepaError) as ei:
+        p.plan(z, s, z, m, m, 1, 1, 8, 2, 1, 0, o)
+    assert ei.value.status == 3                       # weights not loaded
+    bad = bytearray(binding.pack_weights(pc, synthetic.make_weights(pc)))
+    bad[8:12] = (3).to_bytes(4, "little")             # wrong layer count in the header
+    assert p.load_blob(bytes(bad)) == 2
+    p.load_weights(synthetic.make_weights(pc))
+    with pytest.raises(JepaError) as ei:
+        p.plan(z, s, z, m, m, 1, 1, 8, 9, 1, 0, o)    # K > N
+    assert ei.value.status == 1
+    with pytest.raises(JepaError) as ei:
+        p.plan(z, s, z, m, m, 1, 2, 8, 2, 1, 0, o)    # H > max_horizon
+    assert ei.value.status == 2
+    R, L = 2, pc.layers
+    per_pass = 1 + 7 * L + 3        # assemble; 7 per layer; final LN, out-projection, energy
+    # seed + context projection + R x (sample, pass, select/refit) + winner
+    assert p.kernel_count(1, 1, 64, 8, R) == 1 + 1 + R * (1 + per_pass + 1) + 1
+    p.close()
