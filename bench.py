@@ -295,10 +295,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="full", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--candidates", type=int, default=0,
+                    help="override N (and K = N/10) of the workload: small cases for ncu captures")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     wl = synthetic.WORKLOADS[args.workload]
+    if args.candidates:
+        import dataclasses
+        wl = dataclasses.replace(wl, N=args.candidates, K=max(1, args.candidates // 10))
     if args.impl == "reference":
         run_reference(args, wl)
     else:

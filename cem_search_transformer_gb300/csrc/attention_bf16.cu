@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
   uint32_t qf[4][4];
   const int g = lane >> 2, tq = lane & 3;
 
+  // warps whose 16 query rows all lie past T only help with the loads
+  const bool active = (qt * BQ + warp * 16) < T;
   for (int j = 0; j < nkv; ++j) {
     if (j + 1 < nkv) {
       load_kv(j + 1, (j + 1) & 1);
@@ -114,6 +116,15 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
       cp_async_wait<0>();
     }
     __syncthreads();
+    if (!active) {
+      __syncthreads();
+      continue;
+    }
+    // key blocks of 8 (S) and 16 (P V) that hold at least one valid key of this tile; the
+    // skipped ones would contribute exp(-inf) = 0 exactly
+    const int kv_left = Lk - j * BKV;
+    const int nbv = kv_left >= BKV ? 8 : (kv_left + 7) / 8;
+    const int kcv = kv_left >= BKV ? 4 : (kv_left + 15) / 16;
     if (j == 0) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
@@ -129,6 +140,7 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
     for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
       for (int nb = 0; nb < 8; nb += 2) {
+        if (nb >= nbv) continue;
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(b0, b1, b2, b3,
                     Kst + (nb * 8 + ((lane >> 4) << 3) + (lane & 7)) * LD + kk * 16 +
@@ -177,6 +189,7 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
     }
 #pragma unroll
     for (int kc = 0; kc < 4; ++kc) {
+      if (kc >= kcv) continue;
       uint32_t a[4];
       a[0] = pack_bf16(s[2 * kc][0], s[2 * kc][1]);
       a[1] = pack_bf16(s[2 * kc][2], s[2 * kc][3]);
@@ -199,6 +212,7 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
     l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
     l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
   }
+  if (!active) return;
   const float inv0 = 1.f / l_run[0], inv1 = 1.f / l_run[1];
   const int t0 = qt * BQ + warp * 16 + g, t1 = t0 + 8;
   bf16* ob = o + (long long)cand * T * d + h * HD;

@@ -51,124 +51,101 @@ struct Epilogue {
   int P;                 // rows per candidate
   int cand0;             // global candidate index of local candidate 0
   int cands_per_problem; // N of the plan (candidate -> problem)
-  float* partial;        // [M, ntiles] per-tile sums of |z - goal|
-  int ntiles;
+  float* partial;        // [M, ntiles] per-tile (and per column half) sums of |z - goal|
+  int ntiles;            // partial sums per row (energy finalisation adds all of them)
 };
 
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
 
-// Apply the epilogue to `n` consecutive accumulators v[0..n) of row r starting at
-// column c (c, n multiples of 4 except at the matrix edge; the run never crosses
-// `split`). Returns this run's sum of |z - goal| for EPI_OUTPROJ (0 otherwise).
-template <int RUN>
-__device__ __forceinline__ float epilogue_run(const Epilogue& e, int r, int c, float* v, int n,
-                                              int N) {
-  if (e.bias) {
-#pragma unroll
-    for (int i = 0; i < RUN; ++i)
-      if (i < n) v[i] += __ldg(e.bias + c + i);
+__device__ __forceinline__ float4 gelu4(float4 v) {
+  return make_float4(gelu_erf(v.x), gelu_erf(v.y), gelu_erf(v.z), gelu_erf(v.w));
+}
+
+// Per-row addressing, computed once per output row. Meaning by mode (a < 0: row >= M):
+//   STORE/GELU: a = out0 row offset, b = out1 row offset (elements)
+//   RESID:      a = x row offset
+//   INPROJ:     a = x row offset,   b = pos row offset
+//   OUTPROJ:    a = r * N (zpred / zhat row), b = goal row offset
+struct EpiRow {
+  long long a, b;
+};
+
+__device__ __forceinline__ EpiRow epi_row(const Epilogue& e, int r, int M, int N) {
+  EpiRow w;
+  w.a = -1;
+  w.b = 0;
+  if (r >= M) return w;
+  if (e.mode == EPI_STORE || e.mode == EPI_GELU) {
+    w.a = map_row(e.map0, r) * e.ld0;
+    if (e.out1) w.b = map_row(e.map1, r) * e.ld1;
+  } else if (e.mode == EPI_RESID) {
+    w.a = map_row(e.map0, r) * e.ld0;
+  } else if (e.mode == EPI_INPROJ) {
+    w.a = map_row(e.map0, r) * e.ld0;
+    w.b = (long long)(r % e.map0.rpg + e.pos_off) * N;
+  } else {
+    w.a = (long long)r * N;
+    if (e.goal) {
+      const int cand = e.cand0 + r / e.P;
+      const int b = cand / e.cands_per_problem;
+      w.b = ((long long)b * e.P + (r % e.P)) * N;
+    }
   }
-  const bool full = (n == RUN);
-  if (e.mode == EPI_GELU) {
-#pragma unroll
-    for (int i = 0; i < RUN; ++i) v[i] = gelu_erf(v[i]);
+  return w;
+}
+
+__device__ __forceinline__ void store4(void* base, long long off, int bf, float4 v) {
+  if (bf) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(base) + off) = u;
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + off) = v;
+  }
+}
+
+// Apply the epilogue to the 4 accumulators of columns c..c+3 (c % 4 == 0, c + 3 < N) of the
+// row described by w. Requires N, ld0, ld1 and split to be multiples of 4 and 16-byte
+// aligned buffers. Returns |z - goal| summed over the 4 columns (EPI_OUTPROJ with goal).
+__device__ __forceinline__ float epi_apply4(const Epilogue& e, const EpiRow& w, int c, float4 v) {
+  if (e.bias) {
+    const float4 bb = __ldg(reinterpret_cast<const float4*>(e.bias + c));
+    v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
   }
   if (e.mode == EPI_STORE || e.mode == EPI_GELU) {
-    void* base;
-    long long row;
-    int col, ld;
-    if (c >= e.split) {
-      base = e.out1; row = map_row(e.map1, r); col = c - e.split; ld = e.ld1;
-    } else {
-      base = e.out0; row = map_row(e.map0, r); col = c; ld = e.ld0;
-    }
-    if (e.act_bf16) {
-      bf16* o = reinterpret_cast<bf16*>(base) + row * ld + col;
-      if (full && (RUN % 8 == 0) && ((((uintptr_t)o) & 15) == 0)) {
-#pragma unroll
-        for (int i = 0; i < RUN; i += 8) {
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(v[i], v[i + 1]);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
-          __nv_bfloat162 p3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
-          uint4 u;
-          u.x = *reinterpret_cast<uint32_t*>(&p0);
-          u.y = *reinterpret_cast<uint32_t*>(&p1);
-          u.z = *reinterpret_cast<uint32_t*>(&p2);
-          u.w = *reinterpret_cast<uint32_t*>(&p3);
-          *reinterpret_cast<uint4*>(o + i) = u;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < RUN; ++i)
-          if (i < n) o[i] = __float2bfloat16_rn(v[i]);
-      }
-    } else {
-      float* o = reinterpret_cast<float*>(base) + row * ld + col;
-#pragma unroll
-      for (int i = 0; i < RUN; ++i)
-        if (i < n) o[i] = v[i];
-    }
+    if (e.mode == EPI_GELU) v = gelu4(v);
+    if (c >= e.split)
+      store4(e.out1, w.b + (c - e.split), e.act_bf16, v);
+    else
+      store4(e.out0, w.a + c, e.act_bf16, v);
     return 0.f;
   }
-  if (e.mode == EPI_RESID || e.mode == EPI_INPROJ) {
-    float* o = reinterpret_cast<float*>(e.out0) + map_row(e.map0, r) * e.ld0 + c;
-    if (e.mode == EPI_INPROJ) {
-      const float* pr = e.pos + (long long)(r % e.map0.rpg + e.pos_off) * N + c;
-#pragma unroll
-      for (int i = 0; i < RUN; ++i)
-        if (i < n) v[i] += __ldg(pr + i);
-    }
-    if (full && (RUN % 4 == 0) && ((((uintptr_t)o) & 15) == 0)) {
-#pragma unroll
-      for (int i = 0; i < RUN; i += 4) {
-        float4 x = *reinterpret_cast<float4*>(o + i);
-        if (e.mode == EPI_RESID) {
-          x.x += v[i]; x.y += v[i + 1]; x.z += v[i + 2]; x.w += v[i + 3];
-        } else {
-          x = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        }
-        *reinterpret_cast<float4*>(o + i) = x;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < RUN; ++i)
-        if (i < n) o[i] = (e.mode == EPI_RESID) ? o[i] + v[i] : v[i];
-    }
+  if (e.mode == EPI_RESID) {
+    float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out0) + w.a + c);
+    float4 x = *p;
+    x.x += v.x; x.y += v.y; x.z += v.z; x.w += v.w;
+    *p = x;
+    return 0.f;
+  }
+  if (e.mode == EPI_INPROJ) {
+    const float4 pp = __ldg(reinterpret_cast<const float4*>(e.pos + w.b + c));
+    v.x += pp.x; v.y += pp.y; v.z += pp.z; v.w += pp.w;
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out0) + w.a + c) = v;
     return 0.f;
   }
   // EPI_OUTPROJ
-  const long long off = (long long)r * N + c;
-  if (e.zpred) {
-#pragma unroll
-    for (int i = 0; i < RUN; ++i)
-      if (i < n) e.zpred[off + i] = v[i];
-  }
-  if (e.zhat) {
-    if (e.act_bf16) {
-      bf16* o = reinterpret_cast<bf16*>(e.zhat) + off;
-#pragma unroll
-      for (int i = 0; i < RUN; ++i)
-        if (i < n) o[i] = __float2bfloat16_rn(v[i]);
-    } else {
-      float* o = reinterpret_cast<float*>(e.zhat) + off;
-#pragma unroll
-      for (int i = 0; i < RUN; ++i)
-        if (i < n) o[i] = v[i];
-    }
-  }
-  float s = 0.f;
+  const long long off = w.a + c;
+  if (e.zpred) *reinterpret_cast<float4*>(e.zpred + off) = v;
+  if (e.zhat) store4(e.zhat, off, e.act_bf16, v);
   if (e.goal) {
-    const int cand = e.cand0 + r / e.P;
-    const int b = cand / e.cands_per_problem;
-    const float* g = e.goal + ((long long)b * e.P + (r % e.P)) * N + c;
-#pragma unroll
-    for (int i = 0; i < RUN; ++i)
-      if (i < n) s += fabsf(v[i] - __ldg(g + i));
+    const float4 g = __ldg(reinterpret_cast<const float4*>(e.goal + w.b + c));
+    return ((fabsf(v.x - g.x) + fabsf(v.y - g.y)) + fabsf(v.z - g.z)) + fabsf(v.w - g.w);
   }
-  return s;
+  return 0.f;
 }
 
 // ---- kernel launchers (each returns cudaGetLastError() of its launch) ----
@@ -176,13 +153,13 @@ __device__ __forceinline__ float epilogue_run(const Epilogue& e, int r, int c, f
 // tcgen05 / TMA GEMM: out = epilogue(A[M,K] * W[N,K]^T), bf16 in, fp32 accumulate.
 cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                          int* err_flag, int num_sms, cudaStream_t s);
-// Tile width the tensor-core GEMM uses for N (sizes the energy partial buffer).
-int gemm_tc_tile_n(int N);
+// Energy partial sums per row that the tensor-core GEMM writes for an output width N.
+int gemm_tc_partials(int N);
 
 // SIMT fp32 GEMM with the same epilogue (fp32 mode).
 cudaError_t gemm_simt_f32(const float* A, const float* W, int M, int N, int K, const Epilogue& epi,
                           cudaStream_t s);
-int gemm_simt_tile_n();
+int gemm_simt_partials(int N);
 
 // Flash-style attention, bf16 (head dim 64) and fp32 (head dim <= 128, multiple of 32).
 // q [ncand*T, d]; kv [ncand][kv_stride_rows][2d] (K at columns [0,d), V at [d,2d));

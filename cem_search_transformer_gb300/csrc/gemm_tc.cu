@@ -7,8 +7,12 @@
 //   - warp 0: TMA producer (128B-swizzled 128x64 A and BNx64 W boxes into a STAGES-deep ring);
 //   - warp 1: TMEM allocator and single-thread tcgen05.mma issuer (M=128, N=BN, K=16 per
 //     instruction), committing to "smem empty" barriers and to a per-accumulator "full" barrier;
-//   - warps 2-5: epilogue; each reads its 32 TMEM lanes (rows) with tcgen05.ld 32x32b.x32,
-//     applies bias / GELU / residual / position / L1-energy (see common.cuh) and stores.
+//   - warps 2-9: epilogue, two warps per TMEM lane quarter (each takes half of the tile's
+//     columns). A warp reads 32 rows x 32 columns with tcgen05.ld 32x32b.x32 (thread = row),
+//     transposes them through a swizzled 4 KB shared-memory buffer so that each global
+//     access covers contiguous columns of a row, and applies bias / GELU / residual /
+//     position / L1 energy (see common.cuh) four columns at a time. The next chunk's TMEM
+//     load is in flight while the current chunk is processed.
 //   - two TMEM accumulators (2 x BN columns) so the epilogue of tile i overlaps the MMAs of
 //     tile i+1.
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the kernel records an
@@ -23,7 +27,9 @@ namespace jepa {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int NUM_THREADS = 192;                 // 6 warps
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;   // producer, MMA, 8 epilogue warps
+constexpr int STG_FLOATS = 32 * 32;                     // per-warp transpose buffer
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -125,8 +131,10 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
+// Issue a 32-lane x 32-column TMEM load (thread i <- lane i, registers = columns). The
+// registers are only valid after tmem_wait(), which takes them as operands so that no use
+// can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -138,9 +146,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
 }
 
 template <int BN>
@@ -150,9 +166,12 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr int TMEM_COLS = 2 * BN;   // two accumulators; 256 or 512 (power of 2)
-  // ring + barriers (full, empty per stage; tfull, tempty per accumulator; teardown) + slot
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;  // +1024 alignment
+  // ring, epilogue transpose buffers, barriers (full/empty per stage, tfull/tempty per
+  // accumulator, teardown), TMEM address slot + abort flag, 1024 B alignment slack
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + NUM_EPI_WARPS * STG_FLOATS * 4;
+  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 }  // namespace
@@ -187,7 +206,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);   // one arrival per epilogue warp
+      mbar_init(tempty_bar(a), NUM_EPI_WARPS);   // one arrival per epilogue warp
     }
     mbar_init(teardown_bar, 1);
     *abort_flag = 0;
@@ -282,28 +301,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int quarter = warp & 3;             // TMEM lanes quarter*32 .. +31
-    const int row_in_tile = quarter * 32 + lane;
+    // ---------------- epilogue (warps 2..9) ----------------
+    const int ew = warp - 2;
+    const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
+    const int half = ew >> 2;                  // which half of the tile's columns
+    constexpr int HALF = BN / 2;
+    float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * STG_FLOATS;
+    const int cg = lane & 7;                   // column group (4 columns) in the transposed phase
+    const int rsub = lane >> 3;                // rows rsub + 4 i, i = 0..7
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err_flag)) break;
       tc_fence_after();
-      const int m0 = (t / num_n) * BM, n_blk = t % num_n, n0 = n_blk * BN;
-      const int r = m0 + row_in_tile;
-      float esum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c), v);
-        if (r < M && n0 + c < N) esum += epilogue_run<32>(epi, r, n0 + c, v, min(32, N - n0 - c), N);
+      const int m0 = (t / num_n) * BM, n_blk = t % num_n;
+      const int cbase = n_blk * BN + half * HALF;
+      EpiRow rows[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rows[i] = epi_row(epi, m0 + quarter * 32 + rsub + 4 * i, M, N);
+      float esum[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) esum[i] = 0.f;
+      int nvalid = 0;
+      while (nvalid < HALF / 32 && cbase + 32 * nvalid < N) ++nvalid;
+      const uint32_t tbase =
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * HALF);
+      uint32_t r[32];
+      if (nvalid > 0) tmem_ld32_async(tbase, r);
+      for (int j = 0; j < nvalid; ++j) {
+        tmem_wait(r);
+        if (j == nvalid - 1) {
+          // accumulator fully read: hand it back to the MMA warp before finishing the stores
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<float4*>(stg + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+              make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                          __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+        __syncwarp();
+        if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);
+        const int c = cbase + 32 * j + 4 * cg;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = rsub + 4 * i;
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
+          if (rows[i].a >= 0 && c < N) esum[i] += epi_apply4(epi, rows[i], c, v);
+        }
+        __syncwarp();
       }
-      if (epi.mode == EPI_OUTPROJ && epi.goal && r < M)
-        epi.partial[(long long)r * epi.ntiles + n_blk] = esum;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (nvalid == 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+      }
+      if (epi.mode == EPI_OUTPROJ && epi.goal) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float sum = esum[i];
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+          const int row = m0 + quarter * 32 + rsub + 4 * i;
+          if (cg == 0 && row < M)
+            epi.partial[(long long)row * epi.ntiles + 2 * n_blk + half] = sum;
+        }
+      }
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
     }
   }
@@ -349,7 +414,9 @@ static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int bo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int gemm_tc_tile_n(int N) { return (N % 256 == 0 || N > 2048) ? 256 : 128; }
+static int tile_n(int N) { return (N % 256 == 0 || N > 2048) ? 256 : 128; }
+
+int gemm_tc_partials(int N) { return 2 * ((N + tile_n(N) - 1) / tile_n(N)); }
 
 template <int BN>
 static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
@@ -373,9 +440,9 @@ static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, 
 cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                          int* err_flag, int num_sms, cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  if (K <= 0 || K % 8 != 0 || (((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
+  if (K <= 0 || K % 8 != 0 || N % 4 != 0 || (((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
     return cudaErrorInvalidValue;
-  if (gemm_tc_tile_n(N) == 256) return launch_tc<256>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  if (tile_n(N) == 256) return launch_tc<256>(A, W, M, N, K, epi, err_flag, num_sms, s);
   return launch_tc<128>(A, W, M, N, K, epi, err_flag, num_sms, s);
 }
 

@@ -397,7 +397,9 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ A,
   for (int i = 0; i < 4; ++i) {
     const int r = m0 + ty * 4 + i;
     float s = 0.f;
-    if (r < M && c < N) s = epilogue_run<4>(epi, r, c, acc[i], min(4, N - c), N);
+    const EpiRow w = epi_row(epi, r, M, N);
+    if (w.a >= 0 && c < N)
+      s = epi_apply4(epi, w, c, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
     red[ty * 4 + i][tx] = s;
   }
   if (epi.mode == EPI_OUTPROJ && epi.goal) {
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ A,
   }
 }
 
-int gemm_simt_tile_n() { return SG_BN; }
+int gemm_simt_partials(int N) { return (N + SG_BN - 1) / SG_BN; }
 
 cudaError_t gemm_simt_f32(const float* A, const float* W, int M, int N, int K, const Epilogue& epi,
                           cudaStream_t s) {

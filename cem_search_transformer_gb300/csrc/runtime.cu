@@ -182,8 +182,7 @@ jepa_status ensure_workspace(jepa_ctx* ctx, int chunk, int H) {
   const size_t T = tokens(ctx), d = c.width, m = c.mlp, P = c.patch_tokens, E = c.embed_dim;
   const size_t rows = (size_t)chunk * T, ab = act_bytes(ctx);
   const size_t kv_slots = H > 1 ? (size_t)c.layers : 1;
-  const int tile_n = bf16_mode(ctx) ? gemm_tc_tile_n((int)E) : gemm_simt_tile_n();
-  ctx->ntiles = (int)((E + tile_n - 1) / tile_n);
+  ctx->ntiles = bf16_mode(ctx) ? gemm_tc_partials((int)E) : gemm_simt_partials((int)E);
   jepa_status s;
   if ((s = dalloc(ctx, ctx->ws_allocs, &ctx->x, rows * d * 4)) ||
       (s = dalloc(ctx, ctx->ws_allocs, &ctx->xn, rows * d * ab)) ||
