@@ -149,14 +149,19 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
         mma_bf16(s[nb + 1], qf[kk], b2, b3);
       }
     }
+    if (kv_left < BKV) {
+      // only the tile that crosses Lk needs masking
+#pragma unroll
+      for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j * BKV + nb * 8 + 2 * tq + (e & 1) >= Lk) s[nb][e] = -INFINITY;
+    }
+    // running max on raw scores (the positive scale does not change the order); the scale
+    // is folded into one FFMA per element below
     float mx[2] = {m_run[0], m_run[1]};
 #pragma unroll
     for (int nb = 0; nb < 8; ++nb) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = j * BKV + nb * 8 + 2 * tq + (e & 1);
-        s[nb][e] = (key < Lk) ? s[nb][e] * scale_log2 : -INFINITY;
-      }
       mx[0] = fmaxf(mx[0], fmaxf(s[nb][0], s[nb][1]));
       mx[1] = fmaxf(mx[1], fmaxf(s[nb][2], s[nb][3]));
     }
@@ -165,16 +170,18 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
     }
-    const float alpha0 = exp2f(m_run[0] - mx[0]), alpha1 = exp2f(m_run[1] - mx[1]);
+    const float alpha0 = exp2f((m_run[0] - mx[0]) * scale_log2);
+    const float alpha1 = exp2f((m_run[1] - mx[1]) * scale_log2);
     m_run[0] = mx[0];
     m_run[1] = mx[1];
+    const float ms0 = mx[0] * scale_log2, ms1 = mx[1] * scale_log2;
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int nb = 0; nb < 8; ++nb) {
-      s[nb][0] = exp2f(s[nb][0] - mx[0]);
-      s[nb][1] = exp2f(s[nb][1] - mx[0]);
-      s[nb][2] = exp2f(s[nb][2] - mx[1]);
-      s[nb][3] = exp2f(s[nb][3] - mx[1]);
+      s[nb][0] = exp2f(fmaf(s[nb][0], scale_log2, -ms0));
+      s[nb][1] = exp2f(fmaf(s[nb][1], scale_log2, -ms0));
+      s[nb][2] = exp2f(fmaf(s[nb][2], scale_log2, -ms1));
+      s[nb][3] = exp2f(fmaf(s[nb][3], scale_log2, -ms1));
       rs0 += s[nb][0] + s[nb][1];
       rs1 += s[nb][2] + s[nb][3];
     }

@@ -55,8 +55,23 @@ struct Epilogue {
   int ntiles;            // partial sums per row (energy finalisation adds all of them)
 };
 
+// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.26:
+// erf(|x|) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2), t = 1 / (1 + p |x|),
+// |error| <= 1.5e-7; odd in x. Evaluated with the fast reciprocal and exponential.
+__device__ __forceinline__ float erf_as7126(float x) {
+  const float ax = fabsf(x);
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+  float p = fmaf(1.061405429f, t, -1.453152027f);
+  p = fmaf(p, t, 1.421413741f);
+  p = fmaf(p, t, -0.284496736f);
+  p = fmaf(p, t, 0.254829592f);
+  const float y = fmaf(-p * t, __expf(-ax * ax), 1.0f);
+  return copysignf(y, x);
+}
+
+// GELU with the Gaussian CDF written through erf: x * (1 + erf(x / sqrt 2)) / 2.
 __device__ __forceinline__ float gelu_erf(float x) {
-  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+  return 0.5f * x * (1.0f + erf_as7126(x * 0.70710678118654752f));
 }
 
 __device__ __forceinline__ float4 gelu4(float4 v) {
@@ -108,14 +123,30 @@ __device__ __forceinline__ void store4(void* base, long long off, int bf, float4
   }
 }
 
-// Apply the epilogue to the 4 accumulators of columns c..c+3 (c % 4 == 0, c + 3 < N) of the
-// row described by w. Requires N, ld0, ld1 and split to be multiples of 4 and 16-byte
-// aligned buffers. Returns |z - goal| summed over the 4 columns (EPI_OUTPROJ with goal).
-__device__ __forceinline__ float epi_apply4(const Epilogue& e, const EpiRow& w, int c, float4 v) {
-  if (e.bias) {
-    const float4 bb = __ldg(reinterpret_cast<const float4*>(e.bias + c));
-    v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
+// The per-element global operand of a mode (residual x, position row or goal row) for
+// columns c..c+3, loaded separately so callers can issue it ahead of the accumulator.
+__device__ __forceinline__ float4 epi_load4(const Epilogue& e, const EpiRow& w, int c) {
+  if (w.a >= 0) {
+    if (e.mode == EPI_RESID)
+      return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.out0) + w.a + c);
+    if (e.mode == EPI_INPROJ) return __ldg(reinterpret_cast<const float4*>(e.pos + w.b + c));
+    if (e.mode == EPI_OUTPROJ && e.goal)
+      return __ldg(reinterpret_cast<const float4*>(e.goal + w.b + c));
   }
+  return make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ float4 epi_bias4(const Epilogue& e, int c) {
+  return e.bias ? __ldg(reinterpret_cast<const float4*>(e.bias + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Apply the epilogue to the 4 accumulators of columns c..c+3 (c % 4 == 0, c + 3 < N) of the
+// row described by w, given that row's bias and operand from epi_bias4 / epi_load4.
+// Requires N, ld0, ld1 and split to be multiples of 4 and 16-byte aligned buffers. Returns
+// |z - goal| summed over the 4 columns (EPI_OUTPROJ with goal).
+__device__ __forceinline__ float epi_apply4(const Epilogue& e, const EpiRow& w, int c, float4 v,
+                                            float4 bb, float4 op) {
+  v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
   if (e.mode == EPI_STORE || e.mode == EPI_GELU) {
     if (e.mode == EPI_GELU) v = gelu4(v);
     if (c >= e.split)
@@ -124,16 +155,9 @@ __device__ __forceinline__ float epi_apply4(const Epilogue& e, const EpiRow& w, 
       store4(e.out0, w.a + c, e.act_bf16, v);
     return 0.f;
   }
-  if (e.mode == EPI_RESID) {
-    float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out0) + w.a + c);
-    float4 x = *p;
-    x.x += v.x; x.y += v.y; x.z += v.z; x.w += v.w;
-    *p = x;
-    return 0.f;
-  }
-  if (e.mode == EPI_INPROJ) {
-    const float4 pp = __ldg(reinterpret_cast<const float4*>(e.pos + w.b + c));
-    v.x += pp.x; v.y += pp.y; v.z += pp.z; v.w += pp.w;
+  if (e.mode == EPI_RESID || e.mode == EPI_INPROJ) {
+    // residual: x + (acc + bias); in-projection: (acc + bias) + pos
+    v.x += op.x; v.y += op.y; v.z += op.z; v.w += op.w;
     *reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out0) + w.a + c) = v;
     return 0.f;
   }
@@ -141,11 +165,14 @@ __device__ __forceinline__ float epi_apply4(const Epilogue& e, const EpiRow& w, 
   const long long off = w.a + c;
   if (e.zpred) *reinterpret_cast<float4*>(e.zpred + off) = v;
   if (e.zhat) store4(e.zhat, off, e.act_bf16, v);
-  if (e.goal) {
-    const float4 g = __ldg(reinterpret_cast<const float4*>(e.goal + w.b + c));
-    return ((fabsf(v.x - g.x) + fabsf(v.y - g.y)) + fabsf(v.z - g.z)) + fabsf(v.w - g.w);
-  }
+  if (e.goal)
+    return ((fabsf(v.x - op.x) + fabsf(v.y - op.y)) + fabsf(v.z - op.z)) + fabsf(v.w - op.w);
   return 0.f;
+}
+
+// Convenience form that loads its own bias and operand.
+__device__ __forceinline__ float epi_apply4(const Epilogue& e, const EpiRow& w, int c, float4 v) {
+  return epi_apply4(e, w, c, v, epi_bias4(e, c), epi_load4(e, w, c));
 }
 
 // ---- kernel launchers (each returns cudaGetLastError() of its launch) ----

@@ -176,7 +176,7 @@ struct Cfg {
 
 }  // namespace
 
-template <int BN>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int M, int N, int K, Epilogue epi, int* err_flag) {
@@ -309,26 +309,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * STG_FLOATS;
     const int cg = lane & 7;                   // column group (4 columns) in the transposed phase
     const int rsub = lane >> 3;                // rows rsub + 4 i, i = 0..7
+    constexpr bool kStore = (MODE == EPI_STORE || MODE == EPI_GELU);
+    constexpr bool kResid = (MODE == EPI_RESID);
+    constexpr bool kGeneric = !kStore && !kResid;
+    const bool has_operand = kResid || MODE == EPI_INPROJ || (MODE == EPI_OUTPROJ && epi.goal != nullptr);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err_flag)) break;
-      tc_fence_after();
+      // row addressing and the first chunk's global operands are prepared before the
+      // accumulator is ready, so their latency hides behind this tile's MMAs
       const int m0 = (t / num_n) * BM, n_blk = t % num_n;
       const int cbase = n_blk * BN + half * HALF;
-      EpiRow rows[8];
+      const int row0 = m0 + quarter * 32 + rsub;
+      // per-row element offsets: a = destination (out0 / x), b = out1 (STORE) or generic use
+      long long ra[8], rb[8];
+      uint32_t vmask = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rows[i] = epi_row(epi, m0 + quarter * 32 + rsub + 4 * i, M, N);
+      for (int i = 0; i < 8; ++i) {
+        const int r = row0 + 4 * i;
+        if (r < M) vmask |= 1u << i;
+        if constexpr (kStore) {
+          ra[i] = map_row(epi.map0, r) * epi.ld0;
+          rb[i] = epi.out1 ? map_row(epi.map1, r) * epi.ld1 : 0;
+        } else if constexpr (kResid) {
+          ra[i] = map_row(epi.map0, r) * epi.ld0;
+          rb[i] = 0;
+        } else {
+          const EpiRow w = epi_row(epi, r, M, N);
+          ra[i] = w.a;
+          rb[i] = w.b;
+        }
+      }
       float esum[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) esum[i] = 0.f;
       int nvalid = 0;
       while (nvalid < HALF / 32 && cbase + 32 * nvalid < N) ++nvalid;
+      float4 nxt[8], nbias = make_float4(0.f, 0.f, 0.f, 0.f);
+      auto fetch = [&](int c) {
+        const bool ok = c < N;
+        nbias = ok ? epi_bias4(epi, c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (kResid) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            nxt[i] = (ok && ((vmask >> i) & 1))
+                         ? *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(epi.out0) + ra[i] + c)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if constexpr (kGeneric) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            EpiRow w;
+            w.a = ((vmask >> i) & 1) ? ra[i] : -1;
+            w.b = rb[i];
+            nxt[i] = (ok && has_operand) ? epi_load4(epi, w, c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      };
+      if (nvalid > 0) fetch(cbase + 4 * cg);
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err_flag)) break;
+      tc_fence_after();
       const uint32_t tbase =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * HALF);
       uint32_t r[32];
       if (nvalid > 0) tmem_ld32_async(tbase, r);
-      for (int j = 0; j < nvalid; ++j) {
+#pragma unroll
+      for (int j = 0; j < HALF / 32; ++j) {
+        if (j >= nvalid) break;
         tmem_wait(r);
         if (j == nvalid - 1) {
           // accumulator fully read: hand it back to the MMA warp before finishing the stores
@@ -343,12 +389,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                           __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
         __syncwarp();
         if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);
-        const int c = cbase + 32 * j + 4 * cg;
+        const int cchunk = cbase + 32 * j;
+        const int c = cchunk + 4 * cg;
+        const bool col_ok = c < N;
+        float4 cur[8];
+        const float4 bb = nbias;
+        if constexpr (!kStore) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+        }
+        if (j + 1 < nvalid) fetch(c + 32);   // next chunk's operands while this one is processed
+        // the whole 32-column chunk goes to one destination (split is a multiple of 32)
+        const bool second = kStore && cchunk >= epi.split;
+        const int col = second ? c - epi.split : c;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int rr = rsub + 4 * i;
-          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
-          if (rows[i].a >= 0 && c < N) esum[i] += epi_apply4(epi, rows[i], c, v);
+          float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
+          if (!(((vmask >> i) & 1) && col_ok)) continue;
+          v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
+          if constexpr (kStore) {
+            if (MODE == EPI_GELU) v = gelu4(v);
+            const long long off = (second ? rb[i] : ra[i]) + col;
+            if (epi.act_bf16) {
+              __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+              __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+              uint2 u;
+              u.x = *reinterpret_cast<uint32_t*>(&lo);
+              u.y = *reinterpret_cast<uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(second ? epi.out1 : epi.out0) + off) = u;
+            } else {
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(second ? epi.out1 : epi.out0) + off) = v;
+            }
+          } else if constexpr (kResid) {
+            float4 x = cur[i];
+            x.x += v.x; x.y += v.y; x.z += v.z; x.w += v.w;
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(epi.out0) + ra[i] + c) = x;
+          } else {
+            EpiRow w;
+            w.a = ra[i];
+            w.b = rb[i];
+            esum[i] += epi_apply4(epi, w, c, v, make_float4(0.f, 0.f, 0.f, 0.f), cur[i]);
+          }
         }
         __syncwarp();
       }
@@ -357,16 +439,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(acc));
       }
-      if (epi.mode == EPI_OUTPROJ && epi.goal) {
+      if constexpr (MODE == EPI_OUTPROJ) {
+        if (epi.goal) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float sum = esum[i];
-          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-          const int row = m0 + quarter * 32 + rsub + 4 * i;
-          if (cg == 0 && row < M)
-            epi.partial[(long long)row * epi.ntiles + 2 * n_blk + half] = sum;
+          for (int i = 0; i < 8; ++i) {
+            float sum = esum[i];
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            const int row = row0 + 4 * i;
+            if (cg == 0 && row < M)
+              epi.partial[(long long)row * epi.ntiles + 2 * n_blk + half] = sum;
+          }
         }
       }
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
@@ -418,14 +502,14 @@ static int tile_n(int N) { return (N % 256 == 0 || N > 2048) ? 256 : 128; }
 
 int gemm_tc_partials(int N) { return 2 * ((N + tile_n(N) - 1) / tile_n(N)); }
 
-template <int BN>
+template <int BN, int MODE>
 static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                              int* err_flag, int num_sms, cudaStream_t s) {
   using C = Cfg<BN>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -433,8 +517,21 @@ static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, 
   if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, W, N, K, BN)) return cudaErrorInvalidValue;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  k_gemm_tc<BN><<<grid, NUM_THREADS, C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  k_gemm_tc<BN, MODE><<<grid, NUM_THREADS, C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
   return cudaGetLastError();
+}
+
+template <int BN>
+static cudaError_t launch_mode(const bf16* A, const bf16* W, int M, int N, int K,
+                               const Epilogue& epi, int* err_flag, int num_sms, cudaStream_t s) {
+  switch (epi.mode) {
+    case EPI_STORE: return launch_tc<BN, EPI_STORE>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_GELU: return launch_tc<BN, EPI_GELU>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_RESID: return launch_tc<BN, EPI_RESID>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_INPROJ: return launch_tc<BN, EPI_INPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_OUTPROJ: return launch_tc<BN, EPI_OUTPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
@@ -442,8 +539,9 @@ cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, cons
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (K <= 0 || K % 8 != 0 || N % 4 != 0 || (((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
     return cudaErrorInvalidValue;
-  if (tile_n(N) == 256) return launch_tc<256>(A, W, M, N, K, epi, err_flag, num_sms, s);
-  return launch_tc<128>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  if (epi.mode == EPI_STORE && (epi.split % 32) != 0) return cudaErrorInvalidValue;
+  if (tile_n(N) == 256) return launch_mode<256>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  return launch_mode<128>(A, W, M, N, K, epi, err_flag, num_sms, s);
 }
 
 }  // namespace jepa

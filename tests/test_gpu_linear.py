@@ -41,3 +41,20 @@ def test_linear_bf16_matches_matmul(planner, M, N, K, gelu):
     got = host(out)
     scale = np.sqrt(K) * 0.05 + 1.0
     assert np.max(np.abs(got - ref)) < 2e-5 * scale * 10, np.max(np.abs(got - ref))
+
+
+def test_gelu_epilogue_against_exact_erf(planner):
+    """GELU of the GEMM epilogue (erf by Abramowitz & Stegun 7.1.26) against the exact-erf
+    GELU: with W = I the output is gelu(A) for bf16-representable A over [-8, 8]."""
+    K = N = 64
+    M = 2048
+    x = np.linspace(-8, 8, M * K).astype(np.float32).reshape(M, K)
+    A = predictor.round_to_bf16(x)
+    W = np.eye(N, K, dtype=np.float32)
+    out = torch.zeros(M, N, device="cuda")
+    planner.linear_bf16(cuda(_bf16_bits(A).astype(np.int16)), cuda(_bf16_bits(W).astype(np.int16)),
+                        None, M, N, K, 1, out)
+    planner.sync_check()
+    ref = predictor.gelu(A.astype(np.float64))
+    err = np.abs(host(out) - ref)
+    assert np.max(err / np.maximum(1.0, np.abs(ref))) < 2e-6, np.max(err)
