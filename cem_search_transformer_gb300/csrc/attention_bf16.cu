@@ -48,6 +48,12 @@ __device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// 2^x on the special-function unit (flush-to-zero; relative error ~2^-22)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
@@ -79,15 +85,22 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
     else
       *reinterpret_cast<uint4*>(dst) = zero;
   }
+  // each thread copies 16-byte chunk (tid & 7) of key rows (tid >> 3) + 16 s, s = 0..3
+  const int ld_row = threadIdx.x >> 3, ld_ch = threadIdx.x & 7;
+  const bf16* kg = kb + (long long)ld_row * 2 * d + ld_ch * 8;
+  const long long key_step = 16LL * 2 * d;    // 16 key rows
+  const int sm_off = ld_row * LD + ld_ch * 8;
   auto load_kv = [&](int j, int st) {
-    for (int i = threadIdx.x; i < BKV * (HD / 8); i += blockDim.x) {
-      const int r = i >> 3, ch = i & 7;
-      const int key = j * BKV + r;
-      bf16* dk = Ks[st] + r * LD + ch * 8;
-      bf16* dv = Vs[st] + r * LD + ch * 8;
-      if (key < Lk) {
-        cp_async16(dk, kb + (long long)key * 2 * d + ch * 8);
-        cp_async16(dv, vb + (long long)key * 2 * d + ch * 8);
+    const bf16* g0 = kg + (long long)j * BKV * 2 * d;
+    const int key0 = j * BKV + ld_row;
+#pragma unroll
+    for (int s2 = 0; s2 < BKV / 16; ++s2) {
+      bf16* dk = Ks[st] + sm_off + s2 * 16 * LD;
+      bf16* dv = Vs[st] + sm_off + s2 * 16 * LD;
+      if (key0 + 16 * s2 < Lk) {
+        const bf16* gk = g0 + s2 * key_step;
+        cp_async16(dk, gk);
+        cp_async16(dv, gk + d);
       } else {
         *reinterpret_cast<uint4*>(dk) = zero;
         *reinterpret_cast<uint4*>(dv) = zero;
@@ -170,18 +183,18 @@ __global__ void __launch_bounds__(128) k_attention_bf16(const bf16* __restrict__
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
     }
-    const float alpha0 = exp2f((m_run[0] - mx[0]) * scale_log2);
-    const float alpha1 = exp2f((m_run[1] - mx[1]) * scale_log2);
+    const float alpha0 = ex2((m_run[0] - mx[0]) * scale_log2);
+    const float alpha1 = ex2((m_run[1] - mx[1]) * scale_log2);
     m_run[0] = mx[0];
     m_run[1] = mx[1];
     const float ms0 = mx[0] * scale_log2, ms1 = mx[1] * scale_log2;
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int nb = 0; nb < 8; ++nb) {
-      s[nb][0] = exp2f(fmaf(s[nb][0], scale_log2, -ms0));
-      s[nb][1] = exp2f(fmaf(s[nb][1], scale_log2, -ms0));
-      s[nb][2] = exp2f(fmaf(s[nb][2], scale_log2, -ms1));
-      s[nb][3] = exp2f(fmaf(s[nb][3], scale_log2, -ms1));
+      s[nb][0] = ex2(fmaf(s[nb][0], scale_log2, -ms0));
+      s[nb][1] = ex2(fmaf(s[nb][1], scale_log2, -ms0));
+      s[nb][2] = ex2(fmaf(s[nb][2], scale_log2, -ms1));
+      s[nb][3] = ex2(fmaf(s[nb][3], scale_log2, -ms1));
       rs0 += s[nb][0] + s[nb][1];
       rs1 += s[nb][2] + s[nb][3];
     }

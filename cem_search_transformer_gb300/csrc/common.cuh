@@ -55,23 +55,23 @@ struct Epilogue {
   int ntiles;            // partial sums per row (energy finalisation adds all of them)
 };
 
-// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.26:
-// erf(|x|) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2), t = 1 / (1 + p |x|),
-// |error| <= 1.5e-7; odd in x. Evaluated with the fast reciprocal and exponential.
-__device__ __forceinline__ float erf_as7126(float x) {
-  const float ax = fabsf(x);
-  const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+// GELU with the Gaussian CDF written through erf: x * (1 + erf(x / sqrt 2)) / 2.
+// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.26:
+// erf(|u|) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-u^2), t = 1 / (1 + p |u|),
+// |error| <= 1.5e-7, odd in u; here u = x / sqrt 2 and exp(-u^2) = 2^-(x^2 log2(e) / 2),
+// evaluated with the fast reciprocal and base-2 exponential (max GELU error ~5e-7 abs).
+__device__ __forceinline__ float gelu_erf(float x) {
+  const float au = fabsf(x) * 0.70710678118654752f;
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, au, 1.0f));
   float p = fmaf(1.061405429f, t, -1.453152027f);
   p = fmaf(p, t, 1.421413741f);
   p = fmaf(p, t, -0.284496736f);
   p = fmaf(p, t, 0.254829592f);
-  const float y = fmaf(-p * t, __expf(-ax * ax), 1.0f);
-  return copysignf(y, x);
-}
-
-// GELU with the Gaussian CDF written through erf: x * (1 + erf(x / sqrt 2)) / 2.
-__device__ __forceinline__ float gelu_erf(float x) {
-  return 0.5f * x * (1.0f + erf_as7126(x * 0.70710678118654752f));
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-0.72134752044448170f * x * x));
+  const float erf_abs = fmaf(-p * t, e, 1.0f);
+  const float hx = 0.5f * x;
+  return fmaf(hx, copysignf(erf_abs, x), hx);
 }
 
 __device__ __forceinline__ float4 gelu4(float4 v) {
