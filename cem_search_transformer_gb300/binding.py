@@ -25,7 +25,7 @@ EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string
            "jepa_weight_blob_bytes", "jepa_load_weights", "jepa_sample_actions", "jepa_philox4x32_10",
            "jepa_predictor_forward", "jepa_cem_select_refit", "jepa_cem_plan",
            "jepa_plan_kernel_count", "jepa_linear_bf16", "jepa_profile_enable",
-           "jepa_profile_read", "jepa_sync_check")
+           "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc")
 
 
 class JepaError(RuntimeError):
@@ -76,6 +76,7 @@ def load(path: str = _LIB_PATH):
         "jepa_profile_read": ([P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_int64)], I),
         "jepa_sync_check": ([P, P], I),
+        "jepa_energy_l1_noalloc": ([P, P, I, I, I, I, P, P, ctypes.c_char_p, ctypes.c_size_t], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -117,6 +118,20 @@ def _stream(stream) -> Optional[int]:
         import torch
         return torch.cuda.current_stream().cuda_stream
     return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def energy_l1_noalloc(z_pred, goal, B, N, P, E, energy, stream=None):
+    """L1 energy of predicted frames without any device allocation (see the C header).
+
+    For callers that cannot allocate device memory (a fixed memory budget owned by a host
+    framework, or a control loop that must not allocate mid-episode). Raises JepaError with
+    the library's message on failure, e.g. when B*N*ceil(P/32) exceeds the fixed scratch."""
+    lib = load()
+    buf = ctypes.create_string_buffer(256)
+    st = lib.jepa_energy_l1_noalloc(_ptr(z_pred), _ptr(goal), B, N, P, E, _ptr(energy),
+                                    _stream(stream), buf, len(buf))
+    if st != JEPA_OK:
+        raise JepaError(st, buf.value.decode())
 
 
 class Planner:

@@ -181,6 +181,27 @@ jepa_status jepa_profile_enable(jepa_ctx* ctx, int enable);
 jepa_status jepa_profile_read(jepa_ctx* ctx, double* gemm_ms, double* gemm_flops,
                               int64_t* gemm_launches);
 
+/* L1 energy of already-predicted frames, for callers that cannot allocate device memory
+ * (the planning pages have no counterpart: this is a deployment variant of the energy
+ * step). Typical callers: a process running under a fixed device-memory budget owned by
+ * a host framework, or a real-time control loop that must not pay for, or risk failure
+ * of, an allocation in the middle of an episode. No context is needed and nothing is
+ * allocated: the per-candidate partial sums go to one fixed device array inside this
+ * library, 2^20 floats (4 MiB), which every GPU that loads the library keeps until the
+ * process exits.
+ *   z_pred [B,N,P,E] dev   predicted frames (e.g. the z_pred output of jepa_predictor_forward)
+ *   goal   [B,P,E]   dev
+ *   energy [B,N]     dev   output: mean |z_pred - goal| per candidate
+ *   err, err_len           optional caller buffer for a text description of a failure
+ * Limits: B*N*ceil(P/32) <= 2^20, otherwise JEPA_ERR_SHAPE (split the candidates over
+ * several calls). Runs on the current CUDA device. The first call on a device looks up the
+ * array's device address (once per device), so make that first call before any stream
+ * capture. All calls share the array: calls that can overlap on the GPU (on streams with
+ * no ordering between them) race and can return wrong energies; calls ordered on one
+ * stream are safe. */
+jepa_status jepa_energy_l1_noalloc(const float* z_pred, const float* goal, int B, int N, int P,
+                                   int E, float* energy, void* stream, char* err, size_t err_len);
+
 /* Synchronise `stream`, then report JEPA_ERR_TIMEOUT if a bounded device-side wait in
  * any kernel of this context gave up since the last check (the flag is then cleared). */
 jepa_status jepa_sync_check(jepa_ctx* ctx, void* stream);
