@@ -74,8 +74,56 @@ __device__ __forceinline__ float gelu_erf(float x) {
   return fmaf(hx, copysignf(erf_abs, x), hx);
 }
 
+// Packed fp32 pairs (sm_100-family f32x2 arithmetic): two lanes of math per instruction.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Two GELUs at once: the same A&S 7.1.26 evaluation as gelu_erf, with the polynomial, the
+// exponent argument and the final blend in packed f32x2 arithmetic. The polynomial's
+// coefficients are negated so that 1 - p t e is a single FMA.
+__device__ __forceinline__ float2 gelu2(float x0, float x1) {
+  const float au0 = fabsf(x0) * 0.70710678118654752f, au1 = fabsf(x1) * 0.70710678118654752f;
+  const float t0 = __fdividef(1.0f, fmaf(0.3275911f, au0, 1.0f));
+  const float t1 = __fdividef(1.0f, fmaf(0.3275911f, au1, 1.0f));
+  const unsigned long long T = f2_pack(t0, t1);
+  unsigned long long p = f2_fma(f2_pack(-1.061405429f, -1.061405429f), T,
+                                f2_pack(1.453152027f, 1.453152027f));
+  p = f2_fma(p, T, f2_pack(-1.421413741f, -1.421413741f));
+  p = f2_fma(p, T, f2_pack(0.284496736f, 0.284496736f));
+  p = f2_fma(p, T, f2_pack(-0.254829592f, -0.254829592f));
+  p = f2_mul(p, T);                                             // -(poly * t)
+  const unsigned long long X = f2_pack(x0, x1);
+  const float2 arg = f2_unpack(f2_mul(f2_mul(X, X), f2_pack(-0.72134752044448170f, -0.72134752044448170f)));
+  float e0, e1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(arg.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(arg.y));
+  const float2 ea = f2_unpack(f2_fma(p, f2_pack(e0, e1), f2_pack(1.0f, 1.0f)));
+  const unsigned long long HX = f2_mul(X, f2_pack(0.5f, 0.5f));
+  return f2_unpack(f2_fma(HX, f2_pack(copysignf(ea.x, x0), copysignf(ea.y, x1)), HX));
+}
+
 __device__ __forceinline__ float4 gelu4(float4 v) {
-  return make_float4(gelu_erf(v.x), gelu_erf(v.y), gelu_erf(v.z), gelu_erf(v.w));
+  const float2 a = gelu2(v.x, v.y), b = gelu2(v.z, v.w);
+  return make_float4(a.x, a.y, b.x, b.y);
 }
 
 // Per-row addressing, computed once per output row. Meaning by mode (a < 0: row >= M):

@@ -7,8 +7,9 @@
 //   - warp 0: TMA producer (128B-swizzled 128x64 A and BNx64 W boxes into a STAGES-deep ring);
 //   - warp 1: TMEM allocator and single-thread tcgen05.mma issuer (M=128, N=BN, K=16 per
 //     instruction), committing to "smem empty" barriers and to a per-accumulator "full" barrier;
-//   - warps 2-9: epilogue, two warps per TMEM lane quarter (each takes half of the tile's
-//     columns). A warp reads 32 rows x 32 columns with tcgen05.ld 32x32b.x32 (thread = row),
+//   - warps 2..: epilogue, EW warps in all (8, or 16 for the GELU layer whose erf is the
+//     expensive part), EW/4 warps per TMEM lane quarter, each taking a 4/EW share of the
+//     tile's columns. A warp reads 32 rows x 32 columns with tcgen05.ld 32x32b.x32 (thread = row),
 //     transposes them through a swizzled 4 KB shared-memory buffer so that each global
 //     access covers contiguous columns of a row, and applies bias / GELU / residual /
 //     position / L1 energy (see common.cuh) four columns at a time. The next chunk's TMEM
@@ -27,9 +28,11 @@ namespace jepa {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;   // producer, MMA, 8 epilogue warps
 constexpr int STG_FLOATS = 32 * 32;                     // per-warp transpose buffer
+
+// Epilogue warps per CTA for an epilogue mode, and the CTA size (producer + MMA warps too).
+__host__ __device__ constexpr int epi_warps(int mode) { return mode == EPI_GELU ? 16 : 8; }
+__host__ __device__ constexpr int cta_threads(int mode) { return 64 + 32 * epi_warps(mode); }
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -159,17 +162,17 @@ __device__ __forceinline__ void tmem_wait(uint32_t (&r)[32]) {
                : "memory");
 }
 
-template <int BN>
+template <int BN, int EW>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int STAGES = (BN == 256) ? (EW > 8 ? 3 : 4) : (EW > 8 ? 5 : 6);
   static constexpr int TMEM_COLS = 2 * BN;   // two accumulators; 256 or 512 (power of 2)
   // ring, epilogue transpose buffers, barriers (full/empty per stage, tfull/tempty per
   // accumulator, teardown), TMEM address slot + abort flag, 1024 B alignment slack
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = STG_OFF + NUM_EPI_WARPS * STG_FLOATS * 4;
+  static constexpr int BAR_OFF = STG_OFF + EW * STG_FLOATS * 4;
   static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -177,10 +180,11 @@ struct Cfg {
 }  // namespace
 
 template <int BN, int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(cta_threads(MODE), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int M, int N, int K, Epilogue epi, int* err_flag) {
-  using C = Cfg<BN>;
+  constexpr int EW = epi_warps(MODE);
+  using C = Cfg<BN, EW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), NUM_EPI_WARPS);   // one arrival per epilogue warp
+      mbar_init(tempty_bar(a), EW);   // one arrival per epilogue warp
     }
     mbar_init(teardown_bar, 1);
     *abort_flag = 0;
@@ -304,8 +308,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------- epilogue (warps 2..9) ----------------
     const int ew = warp - 2;
     const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
-    const int half = ew >> 2;                  // which half of the tile's columns
-    constexpr int HALF = BN / 2;
+    const int part = ew >> 2;                  // which share of the tile's columns
+    constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp
     float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * STG_FLOATS;
     const int cg = lane & 7;                   // column group (4 columns) in the transposed phase
     const int rsub = lane >> 3;                // rows rsub + 4 i, i = 0..7
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // row addressing and the first chunk's global operands are prepared before the
       // accumulator is ready, so their latency hides behind this tile's MMAs
       const int m0 = (t / num_n) * BM, n_blk = t % num_n;
-      const int cbase = n_blk * BN + half * HALF;
+      const int cbase = n_blk * BN + part * SPAN;
       const int row0 = m0 + quarter * 32 + rsub;
       // per-row element offsets: a = destination (out0 / x), b = out1 (STORE) or generic use
       long long ra[8], rb[8];
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) esum[i] = 0.f;
       int nvalid = 0;
-      while (nvalid < HALF / 32 && cbase + 32 * nvalid < N) ++nvalid;
+      while (nvalid < SPAN / 32 && cbase + 32 * nvalid < N) ++nvalid;
       float4 nxt[8], nbias = make_float4(0.f, 0.f, 0.f, 0.f);
       auto fetch = [&](int c) {
         const bool ok = c < N;
@@ -369,11 +373,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err_flag)) break;
       tc_fence_after();
       const uint32_t tbase =
-          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + half * HALF);
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + part * SPAN);
       uint32_t r[32];
       if (nvalid > 0) tmem_ld32_async(tbase, r);
 #pragma unroll
-      for (int j = 0; j < HALF / 32; ++j) {
+      for (int j = 0; j < SPAN / 32; ++j) {
         if (j >= nvalid) break;
         tmem_wait(r);
         if (j == nvalid - 1) {
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             sum += __shfl_xor_sync(0xffffffffu, sum, 4);
             const int row = row0 + 4 * i;
             if (cg == 0 && row < M)
-              epi.partial[(long long)row * epi.ntiles + 2 * n_blk + half] = sum;
+              epi.partial[(long long)row * epi.ntiles + (EW / 4) * n_blk + part] = sum;
           }
         }
       }
@@ -500,12 +504,15 @@ static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int bo
 
 static int tile_n(int N) { return (N % 256 == 0 || N > 2048) ? 256 : 128; }
 
-int gemm_tc_partials(int N) { return 2 * ((N + tile_n(N) - 1) / tile_n(N)); }
+// energy partials per row written by the out-projection mode: one per epilogue warp share
+int gemm_tc_partials(int N) {
+  return (epi_warps(EPI_OUTPROJ) / 4) * ((N + tile_n(N) - 1) / tile_n(N));
+}
 
 template <int BN, int MODE>
 static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                              int* err_flag, int num_sms, cudaStream_t s) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, epi_warps(MODE)>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, MODE>,
@@ -517,7 +524,7 @@ static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, 
   if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, W, N, K, BN)) return cudaErrorInvalidValue;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  k_gemm_tc<BN, MODE><<<grid, NUM_THREADS, C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  k_gemm_tc<BN, MODE><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
   return cudaGetLastError();
 }
 
