@@ -25,7 +25,8 @@ EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string
            "jepa_weight_blob_bytes", "jepa_load_weights", "jepa_sample_actions", "jepa_philox4x32_10",
            "jepa_predictor_forward", "jepa_cem_select_refit", "jepa_cem_plan",
            "jepa_plan_kernel_count", "jepa_linear_bf16", "jepa_profile_enable",
-           "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc")
+           "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc",
+           "jepa_attention_bf16")
 
 
 class JepaError(RuntimeError):
@@ -76,6 +77,7 @@ def load(path: str = _LIB_PATH):
         "jepa_profile_read": ([P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_int64)], I),
         "jepa_sync_check": ([P, P], I),
+        "jepa_attention_bf16": ([P, P, P, P, I, I, I, I, I, I, P], I),
         "jepa_energy_l1_noalloc": ([P, P, I, I, I, I, P, P, ctypes.c_char_p, ctypes.c_size_t], I),
     }
     for name, (args, res) in sig.items():
@@ -216,6 +218,11 @@ class Planner:
     def linear_bf16(self, A, W, bias, M, N, K, gelu, out, stream=None):
         self._check(self.lib.jepa_linear_bf16(self.h, _ptr(A), _ptr(W), _ptr(bias), M, N, K,
                                               int(gelu), _ptr(out), _stream(stream)), "linear_bf16")
+
+    def attention_bf16(self, q, kv, out, ncand, T, Lk, kv_rows, heads, d, stream=None):
+        self._check(self.lib.jepa_attention_bf16(self.h, _ptr(q), _ptr(kv), _ptr(out), ncand, T, Lk,
+                                                 kv_rows, heads, d, _stream(stream)),
+                    "attention_bf16")
 
     def profile_enable(self, on: bool):
         self._check(self.lib.jepa_profile_enable(self.h, int(on)), "profile_enable")

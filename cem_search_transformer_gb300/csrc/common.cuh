@@ -236,11 +236,12 @@ cudaError_t gemm_simt_f32(const float* A, const float* W, int M, int N, int K, c
                           cudaStream_t s);
 int gemm_simt_partials(int N);
 
-// Flash-style attention, bf16 (head dim 64) and fp32 (head dim <= 128, multiple of 32).
-// q [ncand*T, d]; kv [ncand][kv_stride_rows][2d] (K at columns [0,d), V at [d,2d));
-// queries of the current block attend to key rows [0, Lk) of their candidate.
-cudaError_t attention_bf16(const bf16* q, const bf16* kv, bf16* o, int ncand, int T, int Lk,
-                           long long kv_cand_stride_rows, int heads, int d, cudaStream_t s);
+// Flash-style attention, bf16 on the tensor cores (head dim 64) and fp32 (head dim <= 128,
+// multiple of 32). q [ncand*T, d]; kv [ncand][kv_stride_rows][2d] (K at columns [0,d), V at
+// [d,2d)); queries of the current block attend to key rows [0, Lk) of their candidate.
+cudaError_t attention_tc_bf16(const bf16* q, const bf16* kv, bf16* o, int ncand, int T, int Lk,
+                              long long kv_cand_stride_rows, int heads, int d, int* err_flag,
+                              cudaStream_t s);
 cudaError_t attention_f32(const float* q, const float* kv, float* o, int ncand, int T, int Lk,
                           long long kv_cand_stride_rows, int heads, int d, cudaStream_t s);
 

@@ -195,6 +195,13 @@ jepa_status ensure_workspace(jepa_ctx* ctx, int chunk, int H) {
     free_list(ctx->ws_allocs);
     return s;
   }
+  // cache rows past the current key bound are read (and masked) by the attention kernels:
+  // keep them finite
+  const cudaError_t me = cudaMemset(ctx->kv, 0, kv_slots * chunk * (size_t)H * T * 2 * d * ab);
+  if (me != cudaSuccess) {
+    free_list(ctx->ws_allocs);
+    return fail(ctx, JEPA_ERR_CUDA, "workspace init: %s", cudaGetErrorString(me));
+  }
   ctx->ws_chunk = chunk;
   ctx->ws_H = H;
   return JEPA_OK;
@@ -308,8 +315,8 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
           if ((st = gemm(ctx, ctx->xn, lw.W_qkv, rows, 3 * d, d, e, s, prof))) return st;
         }
         if (bf16_mode(ctx)) {
-          CK(attention_bf16((const bf16*)ctx->q, (const bf16*)kv_slot, (bf16*)ctx->o, nc, T,
-                            (k + 1) * T, kv_stride, heads, d, s));
+          CK(attention_tc_bf16((const bf16*)ctx->q, (const bf16*)kv_slot, (bf16*)ctx->o, nc, T,
+                               (k + 1) * T, kv_stride, heads, d, ctx->dev_err, s));
         } else {
           CK(attention_f32((const float*)ctx->q, (const float*)kv_slot, (float*)ctx->o, nc, T,
                            (k + 1) * T, kv_stride, heads, d, s));
@@ -793,6 +800,23 @@ jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W
   e.ld0 = N;
   CK(gemm_tc_bf16((const bf16*)A, (const bf16*)W, M, N, K, e, ctx->dev_err, ctx->num_sms,
                   (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
+jepa_status jepa_attention_bf16(jepa_ctx* ctx, const uint16_t* q, const uint16_t* kv, uint16_t* out,
+                                int ncand, int T, int Lk, int kv_rows, int heads, int d,
+                                void* stream) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  if (!bf16_mode(ctx)) return fail(ctx, JEPA_ERR_UNSUPPORTED, "attention_bf16 needs a bf16 context");
+  if (bad_ptr(q) || bad_ptr(kv) || bad_ptr(out) || ncand < 1 || ncand > 65535 || T < 1 || Lk < 1 ||
+      Lk > kv_rows || heads < 1 || d != heads * 64)
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "attention_bf16: bad argument");
+  if ((((uintptr_t)q) & 15) || (((uintptr_t)kv) & 15) || (((uintptr_t)out) & 15))
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "attention_bf16: buffers must be 16-byte aligned");
+  CK(cudaSetDevice(ctx->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(attention_tc_bf16((const bf16*)q, (const bf16*)kv, (bf16*)out, ncand, T, Lk, kv_rows, heads, d,
+                       ctx->dev_err, s));
   return JEPA_OK;
 }
 

@@ -172,6 +172,18 @@ jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W
                              const float* bias, int M, int N, int K, int gelu, float* out,
                              void* stream);
 
+/* Block-causal attention of one rollout step as the predictor runs it (bf16 mode): for each
+ * candidate c and head h, queries q[c*T + t, h*64 : h*64+64] attend to cached key / value
+ * rows [0, Lk) of kv[c] (keys at columns [h*64, h*64+64), values at [d + h*64, ...)) with
+ * scale 1/8: out[c*T + t, h*64 + j] = sum_i softmax_i(q . k_i / 8) v_i[j]. (Frame-causal
+ * predictor with a KV cache, the planning page, "Measured on 8x A100".)
+ *   q [ncand*T, d], kv [ncand][kv_rows][2d], out [ncand*T, d]: bf16 bit patterns, dev.
+ *   1 <= Lk <= kv_rows; d = heads * 64; rows of kv past Lk must hold finite values.
+ * Runs the predictor's tcgen05 attention kernel. Needs a bf16 context. */
+jepa_status jepa_attention_bf16(jepa_ctx* ctx, const uint16_t* q, const uint16_t* kv, uint16_t* out,
+                                int ncand, int T, int Lk, int kv_rows, int heads, int d,
+                                void* stream);
+
 /* Kernel-level timing of the predictor GEMMs inside plan graphs. enable != 0 makes graphs
  * captured afterwards record a CUDA event pair around every GEMM launch (graphs captured
  * before keep their state). jepa_profile_read (after the stream is synchronised) returns
