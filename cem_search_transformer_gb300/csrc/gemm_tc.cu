@@ -15,7 +15,10 @@
 //     position / L1 energy (see common.cuh) four columns at a time. The next chunk's TMEM
 //     load is in flight while the current chunk is processed.
 //   - two TMEM accumulators (2 x BN columns) so the epilogue of tile i overlaps the MMAs of
-//     tile i+1.
+//     tile i+1;
+//   - QKV and the residual projections run on CTA pairs (k_gemm_tc2: 256 x 256 tiles with
+//     tcgen05.mma.cta_group::2), the GELU layer and the projections to and from the
+//     embedding space on single CTAs (k_gemm_tc).
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the kernel records an
 // error flag, stops issuing work, waits (bounded) for its own copies and MMAs, frees TMEM
 // and returns.
@@ -50,7 +53,180 @@ struct Cfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+// 2-SM tiles: a CTA pair computes 256 x 256 (each CTA 128 rows, all 256 columns in its TMEM);
+// each CTA stages its own 128 rows of A and its own 128-row half of W per K step.
+template <int EW>
+struct Cfg2 {
+  static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+  static constexpr int B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of the 256 columns
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = EW > 8 ? 5 : 6;
+  static constexpr int TMEM_COLS = 512;         // two 256-column accumulators
+  static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + EW * STG_FLOATS * 4;
+  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
 }  // namespace
+
+// Epilogue of one accumulator tile held in TMEM (rows m0 .. m0+127 of this CTA, columns of
+// tile n_blk), executed by every epilogue warp. Waits for `tfull` (parity), releases the
+// accumulator through `release(tempty)` as soon as its last TMEM load has landed, then
+// finishes the global stores. Returns false if a bounded wait expired.
+template <int BN, int MODE, int EW, typename Release>
+__device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N, int m0, int n_blk,
+                                              uint32_t tmem_acc, uint32_t tfull,
+                                              uint32_t tfull_parity, uint32_t tempty,
+                                              Release release, float* stg, int ew, int warp,
+                                              int lane, volatile int* abort_flag, int* err_flag) {
+  const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
+  const int part = ew >> 2;                  // which share of the tile's columns
+  constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp
+  const int cg = lane & 7;                   // column group (4 columns) in the transposed phase
+  const int rsub = lane >> 3;                // rows rsub + 4 i, i = 0..7
+  constexpr bool kStore = (MODE == EPI_STORE || MODE == EPI_GELU);
+  constexpr bool kResid = (MODE == EPI_RESID);
+  constexpr bool kGeneric = !kStore && !kResid;
+  const bool has_operand = kResid || MODE == EPI_INPROJ || (MODE == EPI_OUTPROJ && epi.goal != nullptr);
+  // row addressing and the first chunk's global operands are prepared before the
+  // accumulator is ready, so their latency hides behind this tile's MMAs
+  const int cbase = n_blk * BN + part * SPAN;
+  const int row0 = m0 + quarter * 32 + rsub;
+  // per-row element offsets: a = destination (out0 / x), b = out1 (STORE) or generic use
+  long long ra[8], rb[8];
+  uint32_t vmask = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = row0 + 4 * i;
+    if (r < M) vmask |= 1u << i;
+    if constexpr (kStore) {
+      ra[i] = map_row(epi.map0, r) * epi.ld0;
+      rb[i] = epi.out1 ? map_row(epi.map1, r) * epi.ld1 : 0;
+    } else if constexpr (kResid) {
+      ra[i] = map_row(epi.map0, r) * epi.ld0;
+      rb[i] = 0;
+    } else {
+      const EpiRow w = epi_row(epi, r, M, N);
+      ra[i] = w.a;
+      rb[i] = w.b;
+    }
+  }
+  float esum[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) esum[i] = 0.f;
+  int nvalid = 0;
+  while (nvalid < SPAN / 32 && cbase + 32 * nvalid < N) ++nvalid;
+  float4 nxt[8], nbias = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fetch = [&](int c) {
+    const bool ok = c < N;
+    nbias = ok ? epi_bias4(epi, c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (kResid) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        nxt[i] = (ok && ((vmask >> i) & 1))
+                     ? *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(epi.out0) + ra[i] + c)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if constexpr (kGeneric) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        EpiRow w;
+        w.a = ((vmask >> i) & 1) ? ra[i] : -1;
+        w.b = rb[i];
+        nxt[i] = (ok && has_operand) ? epi_load4(epi, w, c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+  if (nvalid > 0) fetch(cbase + 4 * cg);
+  if (!mbar_wait(tfull, tfull_parity, abort_flag, err_flag)) return false;
+  tc_fence_after();
+  const uint32_t tbase =
+      tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * SPAN);
+  uint32_t r[32];
+  if (nvalid > 0) tmem_ld32_async(tbase, r);
+#pragma unroll
+  for (int j = 0; j < SPAN / 32; ++j) {
+    if (j >= nvalid) break;
+    tmem_wait(r);
+    if (j == nvalid - 1) {
+      // accumulator fully read: hand it back to the MMA warp before finishing the stores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release(tempty);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<float4*>(stg + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+          make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                      __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+    __syncwarp();
+    if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);
+    const int cchunk = cbase + 32 * j;
+    const int c = cchunk + 4 * cg;
+    const bool col_ok = c < N;
+    float4 cur[8];
+    const float4 bb = nbias;
+    if constexpr (!kStore) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+    }
+    if (j + 1 < nvalid) fetch(c + 32);   // next chunk's operands while this one is processed
+    // the whole 32-column chunk goes to one destination (split is a multiple of 32)
+    const bool second = kStore && cchunk >= epi.split;
+    const int col = second ? c - epi.split : c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = rsub + 4 * i;
+      float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
+      if (!(((vmask >> i) & 1) && col_ok)) continue;
+      v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
+      if constexpr (kStore) {
+        if (MODE == EPI_GELU) v = gelu4(v);
+        const long long off = (second ? rb[i] : ra[i]) + col;
+        if (epi.act_bf16) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&lo);
+          u.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(second ? epi.out1 : epi.out0) + off) = u;
+        } else {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(second ? epi.out1 : epi.out0) + off) = v;
+        }
+      } else if constexpr (kResid) {
+        float4 x = cur[i];
+        x.x += v.x; x.y += v.y; x.z += v.z; x.w += v.w;
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(epi.out0) + ra[i] + c) = x;
+      } else {
+        EpiRow w;
+        w.a = ra[i];
+        w.b = rb[i];
+        esum[i] += epi_apply4(epi, w, c, v, make_float4(0.f, 0.f, 0.f, 0.f), cur[i]);
+      }
+    }
+    __syncwarp();
+  }
+  if (nvalid == 0) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) release(tempty);
+  }
+  if constexpr (MODE == EPI_OUTPROJ) {
+    if (epi.goal) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float sum = esum[i];
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        const int row = row0 + 4 * i;
+        if (cg == 0 && row < M)
+          epi.partial[(long long)row * epi.ntiles + (EW / 4) * n_blk + part] = sum;
+      }
+    }
+  }
+  return true;
+}
 
 template <int BN, int MODE>
 __global__ void __launch_bounds__(cta_threads(MODE), 1)
@@ -178,158 +354,18 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..9) ----------------
+    // ---------------- epilogue (warps 2..) ----------------
     const int ew = warp - 2;
-    const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
-    const int part = ew >> 2;                  // which share of the tile's columns
-    constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp
     float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * STG_FLOATS;
-    const int cg = lane & 7;                   // column group (4 columns) in the transposed phase
-    const int rsub = lane >> 3;                // rows rsub + 4 i, i = 0..7
-    constexpr bool kStore = (MODE == EPI_STORE || MODE == EPI_GELU);
-    constexpr bool kResid = (MODE == EPI_RESID);
-    constexpr bool kGeneric = !kStore && !kResid;
-    const bool has_operand = kResid || MODE == EPI_INPROJ || (MODE == EPI_OUTPROJ && epi.goal != nullptr);
     int acc = 0;
     uint32_t acc_phase = 0;
+    auto release = [](uint32_t bar) { mbar_arrive(bar); };
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      // row addressing and the first chunk's global operands are prepared before the
-      // accumulator is ready, so their latency hides behind this tile's MMAs
       const int m0 = (t / num_n) * BM, n_blk = t % num_n;
-      const int cbase = n_blk * BN + part * SPAN;
-      const int row0 = m0 + quarter * 32 + rsub;
-      // per-row element offsets: a = destination (out0 / x), b = out1 (STORE) or generic use
-      long long ra[8], rb[8];
-      uint32_t vmask = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = row0 + 4 * i;
-        if (r < M) vmask |= 1u << i;
-        if constexpr (kStore) {
-          ra[i] = map_row(epi.map0, r) * epi.ld0;
-          rb[i] = epi.out1 ? map_row(epi.map1, r) * epi.ld1 : 0;
-        } else if constexpr (kResid) {
-          ra[i] = map_row(epi.map0, r) * epi.ld0;
-          rb[i] = 0;
-        } else {
-          const EpiRow w = epi_row(epi, r, M, N);
-          ra[i] = w.a;
-          rb[i] = w.b;
-        }
-      }
-      float esum[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) esum[i] = 0.f;
-      int nvalid = 0;
-      while (nvalid < SPAN / 32 && cbase + 32 * nvalid < N) ++nvalid;
-      float4 nxt[8], nbias = make_float4(0.f, 0.f, 0.f, 0.f);
-      auto fetch = [&](int c) {
-        const bool ok = c < N;
-        nbias = ok ? epi_bias4(epi, c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        if constexpr (kResid) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            nxt[i] = (ok && ((vmask >> i) & 1))
-                         ? *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(epi.out0) + ra[i] + c)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        } else if constexpr (kGeneric) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            EpiRow w;
-            w.a = ((vmask >> i) & 1) ? ra[i] : -1;
-            w.b = rb[i];
-            nxt[i] = (ok && has_operand) ? epi_load4(epi, w, c) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-      };
-      if (nvalid > 0) fetch(cbase + 4 * cg);
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, err_flag)) break;
-      tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + part * SPAN);
-      uint32_t r[32];
-      if (nvalid > 0) tmem_ld32_async(tbase, r);
-#pragma unroll
-      for (int j = 0; j < SPAN / 32; ++j) {
-        if (j >= nvalid) break;
-        tmem_wait(r);
-        if (j == nvalid - 1) {
-          // accumulator fully read: hand it back to the MMA warp before finishing the stores
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<float4*>(stg + lane * 32 + ((k ^ (lane & 7)) << 2)) =
-              make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                          __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
-        __syncwarp();
-        if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);
-        const int cchunk = cbase + 32 * j;
-        const int c = cchunk + 4 * cg;
-        const bool col_ok = c < N;
-        float4 cur[8];
-        const float4 bb = nbias;
-        if constexpr (!kStore) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
-        }
-        if (j + 1 < nvalid) fetch(c + 32);   // next chunk's operands while this one is processed
-        // the whole 32-column chunk goes to one destination (split is a multiple of 32)
-        const bool second = kStore && cchunk >= epi.split;
-        const int col = second ? c - epi.split : c;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = rsub + 4 * i;
-          float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
-          if (!(((vmask >> i) & 1) && col_ok)) continue;
-          v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
-          if constexpr (kStore) {
-            if (MODE == EPI_GELU) v = gelu4(v);
-            const long long off = (second ? rb[i] : ra[i]) + col;
-            if (epi.act_bf16) {
-              __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-              __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-              uint2 u;
-              u.x = *reinterpret_cast<uint32_t*>(&lo);
-              u.y = *reinterpret_cast<uint32_t*>(&hi);
-              *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(second ? epi.out1 : epi.out0) + off) = u;
-            } else {
-              *reinterpret_cast<float4*>(reinterpret_cast<float*>(second ? epi.out1 : epi.out0) + off) = v;
-            }
-          } else if constexpr (kResid) {
-            float4 x = cur[i];
-            x.x += v.x; x.y += v.y; x.z += v.z; x.w += v.w;
-            *reinterpret_cast<float4*>(reinterpret_cast<float*>(epi.out0) + ra[i] + c) = x;
-          } else {
-            EpiRow w;
-            w.a = ra[i];
-            w.b = rb[i];
-            esum[i] += epi_apply4(epi, w, c, v, make_float4(0.f, 0.f, 0.f, 0.f), cur[i]);
-          }
-        }
-        __syncwarp();
-      }
-      if (nvalid == 0) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
-      }
-      if constexpr (MODE == EPI_OUTPROJ) {
-        if (epi.goal) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float sum = esum[i];
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            const int row = row0 + 4 * i;
-            if (cg == 0 && row < M)
-              epi.partial[(long long)row * epi.ntiles + (EW / 4) * n_blk + part] = sum;
-          }
-        }
-      }
+      if (!epilogue_tile<BN, MODE, EW>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
+                                       tfull_bar(acc), acc_phase, tempty_bar(acc), release, stg, ew,
+                                       warp, lane, abort_flag, err_flag))
+        break;
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
     }
   }
@@ -339,6 +375,150 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"((uint32_t)C::TMEM_COLS));
+  }
+}
+
+// 2-SM GEMM: clusters of 2 CTAs walk 256 x 256 output tiles. Both CTAs stage their halves;
+// the leader (cluster rank 0) issues tcgen05.mma.cta_group::2 (M 256, N 256, K 16) and commits
+// to the "smem empty" and "accumulator full" barriers of both CTAs; each CTA's epilogue drains
+// its own 128 rows and releases the accumulator on the leader's barrier. Halving the operand
+// bytes each SM stages per MMA keeps shared-memory traffic within its bandwidth.
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1)
+    k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               int M, int N, int K, Epilogue epi, int* err_flag) {
+  constexpr int EW = epi_warps(MODE);
+  constexpr int BN = 256;
+  using C = Cfg2<EW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+  const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + (2 * C::STAGES + 5) * 8);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_m = (M + 2 * BM - 1) / (2 * BM);
+  const int total = num_m * num_n;
+  const int num_k = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);     // the leader's arrive + both CTAs' transaction bytes
+      mbar_init(empty_bar(s), 1);    // the leader's MMA commit (multicast)
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * EW);   // epilogue warps of both CTAs (used in the leader)
+    }
+    mbar_init(teardown_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), (uint32_t)C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      bool issued_any = false;
+      for (int t = cid; t < total; t += ncl) {
+        const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n0 = (t % num_n) * BN + (int)rank * 128;
+        bool ok = true;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          const uint32_t lfull = map_to_rank(full_bar(stage), 0);
+          if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+          tma_load_2d_pair(sa, &tmA, kb * BK, m0, lfull);
+          tma_load_2d_pair(sa + C::A_BYTES, &tmB, kb * BK, n0, lfull);
+          issued_any = true;
+          if (++stage == C::STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag && issued_any) {
+        // let copies still in flight into this CTA's shared memory land before exiting
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (leader only) ----------------
+      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = cid; t < total && ok; t += ncl) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, err_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+          const uint64_t adesc = desc_sw128(sa);
+          const uint64_t bdesc = desc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          mma_commit_pair_both(empty_bar(stage));
+          if (++stage == C::STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        mma_commit_pair_both(tfull_bar(acc));
+        if (++acc == 2) acc = 0, acc_phase ^= 1u;
+      }
+      mma_commit_pair_local(teardown_bar);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(teardown_bar, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2.., both CTAs) ----------------
+    const int ew = warp - 2;
+    float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * STG_FLOATS;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    auto release = [](uint32_t bar) { mbar_arrive_cluster(bar); };
+    for (int t = cid; t < total; t += ncl) {
+      const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n_blk = t % num_n;
+      if (!epilogue_tile<BN, MODE, EW>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
+                                       tfull_bar(acc), acc_phase, map_to_rank(tempty_bar(acc), 0),
+                                       release, stg, ew, warp, lane, abort_flag, err_flag))
+        break;
+      if (++acc == 2) acc = 0, acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  cluster_sync();   // both CTAs done with TMEM and with each other's barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, (uint32_t)C::TMEM_COLS);
   }
 }
 
@@ -383,12 +563,41 @@ static cudaError_t launch_mode(const bf16* A, const bf16* W, int M, int N, int K
   return cudaErrorInvalidValue;
 }
 
+template <int MODE>
+static cudaError_t launch_tc2(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
+                              int* err_flag, int num_sms, cudaStream_t s) {
+  using C = Cfg2<epi_warps(MODE)>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, W, N, K, 128)) return cudaErrorInvalidValue;
+  const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
+  const int pairs = num_sms / 2;
+  const int grid = 2 * (tiles < pairs ? tiles : pairs);
+  k_gemm_tc2<MODE><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  return cudaGetLastError();
+}
+
 cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                          int* err_flag, int num_sms, cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (K <= 0 || K % 8 != 0 || N % 4 != 0 || (((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
     return cudaErrorInvalidValue;
   if (epi.mode == EPI_STORE && (epi.split % 32) != 0) return cudaErrorInvalidValue;
+  // QKV and the residual projections (N a multiple of 256, many row tiles) run on CTA
+  // pairs; the GELU layer keeps single CTAs, whose 16 epilogue warps need the registers
+  if (N % 256 == 0 && M >= 4 * BM && num_sms >= 2) {
+    switch (epi.mode) {
+      case EPI_STORE: return launch_tc2<EPI_STORE>(A, W, M, N, K, epi, err_flag, num_sms, s);
+      case EPI_RESID: return launch_tc2<EPI_RESID>(A, W, M, N, K, epi, err_flag, num_sms, s);
+      default: break;
+    }
+  }
   if (tile_n(N) == 256) return launch_mode<256>(A, W, M, N, K, epi, err_flag, num_sms, s);
   return launch_mode<128>(A, W, M, N, K, epi, err_flag, num_sms, s);
 }
