@@ -29,6 +29,9 @@ sys.path.insert(0, ROOT)
 from cem_search_transformer_gb300 import synthetic  # noqa: E402
 
 METRIC = "CEM plan-step latency (ms, 800x10) and candidate rollouts/sec, % of roofline"
+# DRAM bytes per launch of the four per-layer GEMMs (QKV, out-projection, MLP up, MLP down)
+# on the full-shape workload, from one ncu capture (profiles/gemm_attention_counters.md).
+GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (429e6 + 1217e6, 1271e6 + 786e6, 434e6 + 1695e6, 2644e6 + 829e6)
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -268,7 +271,9 @@ def run_ours(args, wl):
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": (achieved / peak) if achieved else None,
                          "peak_source": f"{peak_kind} bf16_tflops_sustained (kernel timed inside a long step)",
-                         "traffic": None,
+                         "traffic": (sum(GEMM_DRAM_BYTES_PER_LAUNCH_FULL) / 4
+                                     if args.workload == "full" and not args.candidates else None),
+                         "traffic_unit": "DRAM bytes per launch (mean of the four per-layer GEMMs)",
                          "gemm_share_of_step": (gemm_ms / args.steps) / step_ms if step_ms else None,
                          "gemm_tflop_per_step": step_flops / 1e12 if step_flops else None},
             "e2e": {"value": rollouts / (e2e_ms * 1e-3), "unit": "candidate rollouts/s",
