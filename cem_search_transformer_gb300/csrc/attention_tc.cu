@@ -7,21 +7,24 @@
 // to every cached key row [0, Lk = (k+1) T) of their candidate, so the block-causal mask
 // reduces to the key bound Lk.
 //
-// One CTA = one (128-query tile, head, candidate); adjacent CTAs share a candidate's K/V in
-// L2. 6 warps:
-//   warp 0      TMA producer: Q tile once, then 64-key K and V chunks into a 2-stage ring;
+// Persistent: each CTA walks work items (128-query tile, head, candidate), tile fastest so
+// that the CTAs working on one candidate's K/V at the same time share it in L2. 6 warps:
+//   warp 0      TMA producer: for each item its Q tile (double-buffered) and its 64-key K and
+//               V chunks through a 3-stage ring. It runs ahead across item boundaries, so
+//               the next item's loads hide behind the current item's math;
 //   warp 1      TMEM allocator and single-thread MMA issuer:
 //                 S = Q K^T   (M 128, N 64, K 64; both operands K-major, 128B-swizzled)
 //                 O += P V    (M 128, N 64, K 64; P K-major from shared memory, V read
 //                              MN-major straight from its TMA tile)
 //   warps 2-5   softmax, one query row per thread: read S from TMEM, online max / sum,
-//               write P (bf16, 128B-swizzled) to shared memory, rescale O in TMEM.
-// In the last tile of a block whose T is not a multiple of 128, warps whose rows all lie
-// past T skip the math (see below).
-// TMEM: S in columns [0, 64), O in [64, 128). Keys past Lk are masked to -inf (their P is 0;
-// the K/V rows loaded there are finite: cache rows are zero-initialised or belong to a
-// neighbouring candidate, and rows past the tensor read as zero).
-// All mbarrier waits are bounded (error flag + early exit, as in the GEMM).
+//               write P (bf16, 128B-swizzled) to shared memory, rescale O in TMEM, and at the
+//               end of an item normalise O and store it.
+// TMEM: S in columns [0, 64), O of even items in [64, 128), of odd items in [128, 192), so
+// one item's output read-out overlaps the next item's MMAs. Keys past Lk are masked to
+// -inf (their P is 0; the K/V rows loaded there are finite: cache rows are zero-initialised
+// or belong to a neighbouring candidate, and rows past the tensor read as zero). In the last
+// tile of a block whose T is not a multiple of 128, warps whose rows all lie past T skip the
+// math. All mbarrier waits are bounded (error flag + early exit, as in the GEMM).
 #include "common.cuh"
 #include "tc_common.cuh"
 
@@ -31,23 +34,25 @@ namespace {
 
 using namespace tc;
 
-constexpr int AQ = 128;    // query rows per CTA (MMA M)
+constexpr int AQ = 128;    // query rows per item (MMA M)
 constexpr int AK = 64;     // keys per chunk
 constexpr int AHD = 64;    // head dim
 constexpr int A_THREADS = 192;
-constexpr int KV_STAGES = 2;
+constexpr int KV_STAGES = 3;
 constexpr int Q_BYTES = AQ * AHD * 2;     // 16 KB
 constexpr int KV_BYTES = AK * AHD * 2;    // 8 KB (K or V chunk)
 constexpr int P_BYTES = AQ * AK * 2;      // 16 KB
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_Q = 0;                  // two Q buffers
+constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
 constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
 constexpr int OFF_P = OFF_V + KV_STAGES * KV_BYTES;
 constexpr int OFF_BAR = OFF_P + P_BYTES;
-// q_full, kv_full[2], kv_empty[2], s_full, s_free, p_full, o_full, teardown
-constexpr int NUM_BARS = 10;
+// q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full, s_free, p_full, o_full,
+// o_free[2], teardown
+constexpr int NUM_BARS = 4 + 2 * KV_STAGES + 4 + 2 + 1;
 constexpr int A_SMEM = OFF_BAR + NUM_BARS * 8 + 16 + 1024;
-constexpr uint32_t TMEM_COLS = 128;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr int CTAS_PER_SM = 2;
 
 __device__ __forceinline__ float ex2f(float x) {
   float y;
@@ -57,28 +62,43 @@ __device__ __forceinline__ float ex2f(float x) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(A_THREADS, 3)
+__global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
     k_attention_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                    bf16* __restrict__ o, int T, int Lk, long long kv_stride_rows, int d,
-                   float scale_log2, int* err_flag) {
+                   float scale_log2, int nq, int heads, int ncand, int* err_flag) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + OFF_BAR;
-  const uint32_t q_full = bar;
-  auto kv_full = [&](int s) { return bar + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar + 8u * (3 + s); };
-  const uint32_t s_full = bar + 40, s_free = bar + 48, p_full = bar + 56, o_full = bar + 64;
-  const uint32_t teardown = bar + 72;
+  auto q_full = [&](int b) { return bar + 8u * b; };
+  auto q_empty = [&](int b) { return bar + 8u * (2 + b); };
+  auto kv_full = [&](int s) { return bar + 8u * (4 + s); };
+  auto kv_empty = [&](int s) { return bar + 8u * (4 + KV_STAGES + s); };
+  const uint32_t s_full = bar + 8u * (4 + 2 * KV_STAGES), s_free = s_full + 8, p_full = s_full + 16,
+                 o_full = s_full + 24;
+  auto o_free = [&](int b) { return s_full + 32 + 8u * b; };
+  const uint32_t teardown = s_full + 48;
   uint32_t* tmem_slot = (uint32_t*)(smem + OFF_BAR + NUM_BARS * 8);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
-  const int qt = blockIdx.x, h = blockIdx.y, cand = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = (Lk + AK - 1) / AK;
+  const int nch = (Lk + AK - 1) / AK;                 // key chunks per item
+  const int items = nq * heads * ncand;
+  // items of this CTA: it = blockIdx.x + i * gridDim.x, i = 0, 1, ...
+  const int my_items = blockIdx.x < items ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  auto item_coords = [&](int i, int& qt, int& h, int& cand) {
+    const int it = (int)blockIdx.x + i * (int)gridDim.x;
+    qt = it % nq;
+    h = (it / nq) % heads;
+    cand = it / (nq * heads);
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(q_full(b), 1);
+      mbar_init(q_empty(b), 1);
+      mbar_init(o_free(b), 4);
+    }
     for (int s = 0; s < KV_STAGES; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -97,32 +117,39 @@ __global__ void __launch_bounds__(A_THREADS, 3)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 64;
+  const uint32_t tS = tmem;
+  auto tO = [&](int i) { return tmem + 64u + 64u * (uint32_t)(i & 1); };
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      mbar_expect_tx(q_full, Q_BYTES);
-      tma_load_2d(sb + OFF_Q, &tmQ, h * AHD, cand * T + qt * AQ, q_full);
-      int issued = -1;
-      for (int j = 0; j < nch; ++j) {
-        const int st = j & 1;
-        if (j >= KV_STAGES && !mbar_wait(kv_empty(st), ((j >> 1) - 1) & 1, abort_flag, err_flag))
-          break;
-        const int ky = (int)(cand * kv_stride_rows + (long long)j * AK);
-        mbar_expect_tx(kv_full(st), 2 * KV_BYTES);
-        tma_load_2d(sb + OFF_K + st * KV_BYTES, &tmKV, h * AHD, ky, kv_full(st));
-        tma_load_2d(sb + OFF_V + st * KV_BYTES, &tmKV, d + h * AHD, ky, kv_full(st));
-        issued = j;
+      int g = 0;   // global chunk counter of this CTA
+      bool ok = true;
+      for (int i = 0; i < my_items && ok; ++i) {
+        int qt, h, cand;
+        item_coords(i, qt, h, cand);
+        const int qb = i & 1;
+        if (i >= 2 && !mbar_wait(q_empty(qb), ((i >> 1) - 1) & 1, abort_flag, err_flag)) break;
+        mbar_expect_tx(q_full(qb), Q_BYTES);
+        tma_load_2d(sb + OFF_Q + qb * Q_BYTES, &tmQ, h * AHD, cand * T + qt * AQ, q_full(qb));
+        for (int j = 0; j < nch; ++j, ++g) {
+          const int st = g % KV_STAGES;
+          if (g >= KV_STAGES &&
+              !mbar_wait(kv_empty(st), ((g / KV_STAGES) - 1) & 1, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          const int ky = (int)(cand * kv_stride_rows + (long long)j * AK);
+          mbar_expect_tx(kv_full(st), 2 * KV_BYTES);
+          tma_load_2d(sb + OFF_K + st * KV_BYTES, &tmKV, h * AHD, ky, kv_full(st));
+          tma_load_2d(sb + OFF_V + st * KV_BYTES, &tmKV, d + h * AHD, ky, kv_full(st));
+        }
       }
       if (*abort_flag) {
-        // wait (bounded) for the copies this thread started before the CTA exits
+        // give copies still in flight into this CTA's shared memory time to land
         const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(q_full, 0) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+        while (globaltimer() - t0 < 2000000ull) {
         }
-        for (int j = (issued - 1 > 0 ? issued - 1 : 0); j <= issued; ++j)
-          while (!mbar_try_wait(kv_full(j & 1), (j >> 1) & 1) && globaltimer() - t0 < WAIT_LIMIT_NS) {
-          }
       }
     }
   } else if (warp == 1) {
@@ -130,37 +157,48 @@ __global__ void __launch_bounds__(A_THREADS, 3)
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idS = idesc_bf16(AQ, AK, false);
       constexpr uint32_t idO = idesc_bf16(AQ, AHD, true);
-      bool ok = mbar_wait(q_full, 0, abort_flag, err_flag) &&
-                mbar_wait(kv_full(0), 0, abort_flag, err_flag);
-      const uint64_t qdesc = desc_sw128(sb + OFF_Q);
-      auto issue_s = [&](int j) {
-        const uint64_t kdesc = desc_sw128(sb + OFF_K + (j & 1) * KV_BYTES);
+      const int total = my_items * nch;
+      auto issue_s = [&](int gg) {
+        // the chunk gg belongs to item gg / nch, whose Q sits in buffer (gg / nch) & 1
+        const int ii = gg / nch;
+        const uint64_t qdesc = desc_sw128(sb + OFF_Q + (ii & 1) * Q_BYTES);
+        const uint64_t kdesc = desc_sw128(sb + OFF_K + (gg % KV_STAGES) * KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < AHD / 16; ++kk) mma_bf16_ss(tS, qdesc + 2 * kk, kdesc + 2 * kk, idS, kk > 0);
         mma_commit(s_full);
       };
+      auto ready_s = [&](int gg) {   // operands of S for chunk gg are in shared memory
+        const int ii = gg / nch;
+        if (gg % nch == 0 && !mbar_wait(q_full(ii & 1), (ii >> 1) & 1, abort_flag, err_flag)) return false;
+        return mbar_wait(kv_full(gg % KV_STAGES), (gg / KV_STAGES) & 1, abort_flag, err_flag);
+      };
+      bool ok = total > 0 && ready_s(0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
-      for (int j = 0; j < nch && ok; ++j) {
-        if (j + 1 < nch) {
-          // S is single-buffered: the next chunk's scores go in once the softmax has read S_j
-          if (!mbar_wait(kv_full((j + 1) & 1), ((j + 1) >> 1) & 1, abort_flag, err_flag) ||
-              !mbar_wait(s_free, j & 1, abort_flag, err_flag))
-            break;
+      for (int gg = 0; gg < total && ok; ++gg) {
+        const int ii = gg / nch, j = gg % nch;
+        if (gg + 1 < total) {
+          // S is single-buffered: the next chunk's scores go in once the softmax has read S
+          if (!ready_s(gg + 1) || !mbar_wait(s_free, gg & 1, abort_flag, err_flag)) break;
           tc_fence_after();
-          issue_s(j + 1);
+          issue_s(gg + 1);
         }
-        if (!mbar_wait(p_full, j & 1, abort_flag, err_flag)) break;
+        if (!mbar_wait(p_full, gg & 1, abort_flag, err_flag)) break;
+        // the O buffer of this item was last read out for item ii - 2
+        if (j == 0 && ii >= 2 && !mbar_wait(o_free(ii & 1), ((ii >> 1) - 1) & 1, abort_flag, err_flag))
+          break;
         tc_fence_after();
         const uint64_t pdesc = desc_sw128(sb + OFF_P);
-        const uint64_t vdesc = desc_sw128_mn(sb + OFF_V + (j & 1) * KV_BYTES);
+        const uint64_t vdesc = desc_sw128_mn(sb + OFF_V + (gg % KV_STAGES) * KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < AK / 16; ++kk)  // 16 keys = 16 rows x 128 B = 2048 B per step
-          mma_bf16_ss(tO, pdesc + 2 * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), idO, (j > 0) || (kk > 0));
+          mma_bf16_ss(tO(ii), pdesc + 2 * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), idO,
+                      (j > 0) || (kk > 0));
         mma_commit(o_full);
-        mma_commit(kv_empty(j & 1));
+        mma_commit(kv_empty(gg % KV_STAGES));
+        if (j == nch - 1) mma_commit(q_empty(ii & 1));
       }
       mma_commit(teardown);
       const unsigned long long t0 = globaltimer();
@@ -172,144 +210,161 @@ __global__ void __launch_bounds__(A_THREADS, 3)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // a warp whose 32 query rows all lie past T (last, partial tile) skips the math but keeps
-    // the same barrier sequence, so its arrivals never count toward another chunk's phase
-    const bool active = (qt * AQ + quarter * 32) < T;
-    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nch; ++j) {
-      if (!mbar_wait(s_full, j & 1, abort_flag, err_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (!active) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
-        if (j > 0 && !mbar_wait(o_full, (j - 1) & 1, abort_flag, err_flag)) {
-          ok = false;
-          break;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
-        continue;
-      }
-      uint32_t sa[32], sc[32];
-      tmem_ld32_async(tS + lane_off, sa);
-      tmem_ld32_async(tS + lane_off + 32, sc);
-      tmem_wait(sa);
-      tmem_wait(sc);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      float s[64];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = __uint_as_float(sa[c]);
-        s[32 + c] = __uint_as_float(sc[c]);
-      }
-      const int kv_left = Lk - j * AK;
-      if (kv_left < AK) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c >= kv_left) s[c] = -INFINITY;
-      }
-      // row max as a tree (8 independent chains, then combine)
-      float part[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        part[g] = fmaxf(fmaxf(fmaxf(s[8 * g], s[8 * g + 1]), fmaxf(s[8 * g + 2], s[8 * g + 3])),
-                        fmaxf(fmaxf(s[8 * g + 4], s[8 * g + 5]), fmaxf(s[8 * g + 6], s[8 * g + 7])));
-      }
-      const float cmax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                               fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
-      // The exponent reference m only moves when the row max grows by more than 8 (log2 units):
-      // until then P = 2^(s c - m c) stays <= 256, and since the same m scales the numerator
-      // (O) and the denominator (l), the result is unchanged. Most chunks then skip the O
-      // rescale in TMEM.
-      const bool bump = (m == -INFINITY) || ((cmax - m) * scale_log2 > 8.0f);
-      const float mnew = bump ? fmaxf(m, cmax) : m;
-      const float alpha = ex2f((m - mnew) * scale_log2);   // 1 when m is kept, 0 on the first chunk
-      const float ms = mnew * scale_log2;
-      // the previous P V must be complete before P is overwritten and O is rescaled
-      if (j > 0) {
-        if (!mbar_wait(o_full, (j - 1) & 1, abort_flag, err_flag)) {
+    int g = 0;
+    for (int i = 0; i < my_items && ok; ++i) {
+      int qt, h, cand;
+      item_coords(i, qt, h, cand);
+      // a warp whose 32 query rows all lie past T (last, partial tile) skips the math but
+      // keeps the same barrier sequence, so its arrivals never count toward another phase
+      const bool active = (qt * AQ + quarter * 32) < T;
+      const uint32_t tOi = tO(i);
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nch; ++j, ++g) {
+        if (!mbar_wait(s_full, g & 1, abort_flag, err_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      // exponentiate, sum and store P 8 columns (16 bytes) at a time: 64 bf16 per row, chunk
-      // cc of the 128-byte row stored at position cc ^ (row % 8) (128-byte swizzle)
-      uint8_t* prow = smem + OFF_P + (row >> 3) * 1024 + (row & 7) * 128;
-      float rsp[8];
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float e[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) e[t] = ex2f(fmaf(s[8 * cc + t], scale_log2, -ms));
-        rsp[cc] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(e[0], e[1]);
-        __nv_bfloat162 p1 = __floats2bfloat162_rn(e[2], e[3]);
-        __nv_bfloat162 p2 = __floats2bfloat162_rn(e[4], e[5]);
-        __nv_bfloat162 p3 = __floats2bfloat162_rn(e[6], e[7]);
-        uint4 u;
-        u.x = *reinterpret_cast<uint32_t*>(&p0);
-        u.y = *reinterpret_cast<uint32_t*>(&p1);
-        u.z = *reinterpret_cast<uint32_t*>(&p2);
-        u.w = *reinterpret_cast<uint32_t*>(&p3);
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) = u;
-      }
-      const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
-      l = l * alpha + rs;
-      m = mnew;
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        uint32_t ov[32], ow[32];
-        tmem_ld32_async(tO + lane_off, ov);
-        tmem_ld32_async(tO + lane_off + 32, ow);
-        tmem_wait(ov);
-        tmem_wait(ow);
+        if (!active) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
+          if (j > 0 && !mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full);
+          continue;
+        }
+        uint32_t sa[32], sc[32];
+        tmem_ld32_async(tS + lane_off, sa);
+        tmem_ld32_async(tS + lane_off + 32, sc);
+        tmem_wait(sa);
+        tmem_wait(sc);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        float s[64];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-          ow[c] = __float_as_uint(__uint_as_float(ow[c]) * alpha);
+          s[c] = __uint_as_float(sa[c]);
+          s[32 + c] = __uint_as_float(sc[c]);
         }
-        tmem_st32(tO + lane_off, ov);
-        tmem_st32(tO + lane_off + 32, ow);
-        tmem_st_wait();
+        const int kv_left = Lk - j * AK;
+        if (kv_left < AK) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c >= kv_left) s[c] = -INFINITY;
+        }
+        // row max as a tree (8 independent chains, then combine)
+        float part[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          part[q] = fmaxf(fmaxf(fmaxf(s[8 * q], s[8 * q + 1]), fmaxf(s[8 * q + 2], s[8 * q + 3])),
+                          fmaxf(fmaxf(s[8 * q + 4], s[8 * q + 5]), fmaxf(s[8 * q + 6], s[8 * q + 7])));
+        const float cmax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                                 fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+        // The exponent reference m only moves when the row max grows by more than 8 (log2
+        // units): until then P = 2^(s c - m c) stays <= 256, and since the same m scales the
+        // numerator (O) and the denominator (l), the result is unchanged. Most chunks then
+        // skip the O rescale in TMEM.
+        const bool bump = (m == -INFINITY) || ((cmax - m) * scale_log2 > 8.0f);
+        const float mnew = bump ? fmaxf(m, cmax) : m;
+        const float alpha = ex2f((m - mnew) * scale_log2);   // 1 when m is kept, 0 at j = 0
+        const float ms = mnew * scale_log2;
+        // the previous P V must be complete before P is overwritten and O is rescaled
+        if (j > 0) {
+          if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        // exponentiate, sum and store P 8 columns (16 bytes) at a time: 64 bf16 per row,
+        // chunk cc of the 128-byte row stored at position cc ^ (row % 8) (128-byte swizzle)
+        uint8_t* prow = smem + OFF_P + (row >> 3) * 1024 + (row & 7) * 128;
+        float rsp[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          float e[8];
+          if (8 * cc >= kv_left) {
+            // every key of this group lies past Lk: P is exactly 0
+#pragma unroll
+            for (int t = 0; t < 8; ++t) e[t] = 0.f;
+          } else {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) e[t] = ex2f(fmaf(s[8 * cc + t], scale_log2, -ms));
+          }
+          rsp[cc] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(e[0], e[1]);
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(e[2], e[3]);
+          __nv_bfloat162 p2 = __floats2bfloat162_rn(e[4], e[5]);
+          __nv_bfloat162 p3 = __floats2bfloat162_rn(e[6], e[7]);
+          uint4 u;
+          u.x = *reinterpret_cast<uint32_t*>(&p0);
+          u.y = *reinterpret_cast<uint32_t*>(&p1);
+          u.z = *reinterpret_cast<uint32_t*>(&p2);
+          u.w = *reinterpret_cast<uint32_t*>(&p3);
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) = u;
+        }
+        const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
+        l = l * alpha + rs;
+        m = mnew;
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          uint32_t ov[32], ow[32];
+          tmem_ld32_async(tOi + lane_off, ov);
+          tmem_ld32_async(tOi + lane_off + 32, ow);
+          tmem_wait(ov);
+          tmem_wait(ow);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            ow[c] = __float_as_uint(__uint_as_float(ow[c]) * alpha);
+          }
+          tmem_st32(tOi + lane_off, ov);
+          tmem_st32(tOi + lane_off + 32, ow);
+          tmem_st_wait();
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the MMA
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok && active && mbar_wait(o_full, (nch - 1) & 1, abort_flag, err_flag)) {
+      if (!ok) break;
+      // end of the item: wait for its last P V, normalise O, store, hand the O buffer back
+      if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) break;
       tc_fence_after();
-      const float inv = 1.f / l;
-      const int t = qt * AQ + row;
-      bf16* orow = o + ((long long)cand * T + t) * d + h * AHD;
+      if (active) {
+        const float inv = 1.f / l;
+        const int t = qt * AQ + row;
+        bf16* orow = o + ((long long)cand * T + t) * d + h * AHD;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t ov[32];
-        tmem_ld32_async(tO + lane_off + 32 * hf, ov);
-        tmem_wait(ov);
-        if (t < T) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t ov[32];
+          tmem_ld32_async(tOi + lane_off + 32 * hf, ov);
+          tmem_wait(ov);
+          if (t < T) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 u;
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-            __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-            u.x = *reinterpret_cast<uint32_t*>(&p0);
-            u.y = *reinterpret_cast<uint32_t*>(&p1);
-            u.z = *reinterpret_cast<uint32_t*>(&p2);
-            u.w = *reinterpret_cast<uint32_t*>(&p3);
-            *reinterpret_cast<uint4*>(orow + 32 * hf + c) = u;
+            for (int c = 0; c < 32; c += 8) {
+              uint4 u;
+              __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+              __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+              __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+              __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+              u.x = *reinterpret_cast<uint32_t*>(&p0);
+              u.y = *reinterpret_cast<uint32_t*>(&p1);
+              u.z = *reinterpret_cast<uint32_t*>(&p2);
+              u.w = *reinterpret_cast<uint32_t*>(&p3);
+              *reinterpret_cast<uint4*>(orow + 32 * hf + c) = u;
+            }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free(i & 1));
     }
   }
   tc_fence_before();
@@ -328,20 +383,26 @@ cudaError_t attention_tc_bf16(const bf16* q, const bf16* kv, bf16* o, int ncand,
   const int nq = (T + AQ - 1) / AQ;
   if (d != heads * AHD || d % 8) return cudaErrorInvalidValue;
   static bool attr_done = false;
+  static int num_sms = 0;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          A_SMEM);
     if (e != cudaSuccess) return e;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
     attr_done = true;
   }
   CUtensorMap mq, mkv;
   if (!make_map(&mq, q, ncand * T, d, AQ, AHD) ||
       !make_map(&mkv, kv, (int)(ncand * kv_cand_stride_rows), 2 * d, AK, AHD))
     return cudaErrorInvalidValue;
-  dim3 grid(nq, heads, ncand);
+  const long long items = (long long)nq * heads * ncand;
+  const long long slots = (long long)num_sms * CTAS_PER_SM;
+  const int grid = (int)(items < slots ? items : slots);
   const float scale_log2 = (1.0f / 8.0f) * 1.4426950408889634f;  // 1/sqrt(64) * log2(e)
   k_attention_tc<<<grid, A_THREADS, A_SMEM, s>>>(mq, mkv, o, T, Lk, kv_cand_stride_rows, d,
-                                                  scale_log2, err_flag);
+                                                  scale_log2, nq, heads, ncand, err_flag);
   return cudaGetLastError();
 }
 
