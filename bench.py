@@ -7,6 +7,13 @@ full planning step (all rounds, through jepa_cem_plan). The metric is candidate 
 second (N * R * B / step time); ms per step is reported beside it.
 
   python bench.py [--gpus N --steps K --warmup W --workload NAME --impl ours|reference]
+  python bench.py --closed-loop T [--rounds R] [--warm] [--workload NAME]
+
+The --closed-loop mode times a receding-horizon episode instead ("Further Optimization",
+parts A and B of the planning page): T control steps, each a full plan followed by one
+world-model step that executes the winner's first action, optionally warm-started from
+the previous plan; it prints one JSON line with ms per control step and the L1 distance
+to the goal after every step.
 
 Under torchrun (N > 1) each rank plans its own independent problem (weak scaling, no
 collective on the data path); rank 0 prints one JSON line with the max-over-ranks time.
@@ -293,6 +300,56 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_closed_loop(args, wl):
+    import torch
+    from cem_search_transformer_gb300 import binding, build_lib
+
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pc = wl.predictor
+    B, N, K, R, H, T = wl.B, wl.N, wl.K, wl.rounds, wl.horizon, args.closed_loop
+    planner = binding.Planner(pc, max_horizon=H)
+    planner.load_weights(synthetic.make_weights(pc, seed=0))
+    z0, goal, s0 = synthetic.make_problems(pc, B)
+    mu0, sg0 = synthetic.make_gaussian(pc, B, H)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    dz0, dgoal, ds0, dmu, dsg = t(z0), t(goal), t(s0), t(mu0), t(sg0)
+    acts = torch.zeros(T, B, pc.action_dim, device=dev)
+    dist = torch.zeros(T, B, device=dev)
+    d0 = torch.zeros(B, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    binding.energy_l1_noalloc(dz0, dgoal, B, 1, pc.patch_tokens, pc.embed_dim, d0, stream=stream)
+    run = lambda: planner.closed_loop(dz0, ds0, dgoal, dmu, dsg, B, H, N, K, R, T, args.warm,
+                                      wl.seed, acts, dist, stream=stream)
+    for _ in range(max(1, args.warmup)):
+        run()
+    planner.sync_check(stream)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            run()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    planner.sync_check(stream)
+    ms_episode = ev0.elapsed_time(ev1) / args.steps
+    line = {
+        "metric": "closed-loop control-step latency (plan + world-model step)",
+        "value": ms_episode / T, "unit": "ms per control step", "higher_is_better": False,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16"
+        if pc.precision == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "control_steps": T, "rounds": R,
+                   "warm_start": bool(args.warm)},
+        "distance_start": float(d0.mean().item()),
+        "distance_per_step": [float(x) for x in dist.mean(dim=1).tolist()],
+        "first_action_norm": [float(x) for x in acts[:, 0].norm(dim=1).tolist()],
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    planner.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -302,6 +359,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--candidates", type=int, default=0,
                     help="override N (and K = N/10) of the workload: small cases for ncu captures")
+    ap.add_argument("--rounds", type=int, default=0, help="override the workload's CEM rounds")
+    ap.add_argument("--closed-loop", type=int, default=0, metavar="T",
+                    help="time a T-step receding-horizon episode instead of one plan step")
+    ap.add_argument("--warm", action="store_true", help="warm-start each step (--closed-loop)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -309,7 +370,12 @@ def main():
     if args.candidates:
         import dataclasses
         wl = dataclasses.replace(wl, N=args.candidates, K=max(1, args.candidates // 10))
-    if args.impl == "reference":
+    if args.rounds:
+        import dataclasses
+        wl = dataclasses.replace(wl, rounds=args.rounds)
+    if args.closed_loop:
+        run_closed_loop(args, wl)
+    elif args.impl == "reference":
         run_reference(args, wl)
     else:
         run_ours(args, wl)

@@ -26,7 +26,8 @@ EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string
            "jepa_predictor_forward", "jepa_cem_select_refit", "jepa_cem_plan",
            "jepa_plan_kernel_count", "jepa_linear_bf16", "jepa_profile_enable",
            "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc",
-           "jepa_attention_bf16")
+           "jepa_attention_bf16", "jepa_cem_warm_start", "jepa_world_model_step",
+           "jepa_cem_closed_loop")
 
 
 class JepaError(RuntimeError):
@@ -79,6 +80,9 @@ def load(path: str = _LIB_PATH):
         "jepa_sync_check": ([P, P], I),
         "jepa_attention_bf16": ([P, P, P, P, I, I, I, I, I, I, P], I),
         "jepa_energy_l1_noalloc": ([P, P, I, I, I, I, P, P, ctypes.c_char_p, ctypes.c_size_t], I),
+        "jepa_cem_warm_start": ([P, P, P, P, I, I, P, P, P], I),
+        "jepa_world_model_step": ([P, P, P, P, I, P, P, P, P, P], I),
+        "jepa_cem_closed_loop": ([P, P, P, P, P, P, I, I, I, I, I, I, I, U64, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -208,6 +212,24 @@ class Planner:
             self.h, _ptr(z0), _ptr(state0), _ptr(goal), _ptr(mu0), _ptr(sigma0), B, H, N, K,
             rounds, seed, _ptr(action_out), ctypes.byref(tr) if tr is not None else None,
             _stream(stream)), "cem_plan")
+
+    def warm_start(self, mu_prev, mu_prior, sigma_prior, B, H, mu_out, sigma_out, stream=None):
+        self._check(self.lib.jepa_cem_warm_start(
+            self.h, _ptr(mu_prev), _ptr(mu_prior), _ptr(sigma_prior), B, H, _ptr(mu_out),
+            _ptr(sigma_out), _stream(stream)), "cem_warm_start")
+
+    def world_model_step(self, z, state, action, B, z_next, state_next, goal=None, distance=None,
+                         stream=None):
+        self._check(self.lib.jepa_world_model_step(
+            self.h, _ptr(z), _ptr(state), _ptr(action), B, _ptr(goal), _ptr(z_next),
+            _ptr(state_next), _ptr(distance), _stream(stream)), "world_model_step")
+
+    def closed_loop(self, z0, state0, goal, mu_prior, sigma_prior, B, H, N, K, rounds, steps,
+                    warm, seed, actions_out, distance_out, stream=None):
+        self._check(self.lib.jepa_cem_closed_loop(
+            self.h, _ptr(z0), _ptr(state0), _ptr(goal), _ptr(mu_prior), _ptr(sigma_prior), B, H,
+            N, K, rounds, steps, int(warm), seed, _ptr(actions_out), _ptr(distance_out),
+            _stream(stream)), "cem_closed_loop")
 
     def kernel_count(self, B, H, N, K, rounds) -> int:
         c = ctypes.c_int64()

@@ -333,6 +333,42 @@ cudaError_t winner_action(const float* actions, const int* winner, int B, int N,
   return cudaGetLastError();
 }
 
+// Receding-horizon warm start ("Further Optimization", B. Warm-started CEM): the last
+// round's mean loses its executed first step, steps 1..H-1 move to 0..H-2, the new last
+// step and every width come from the prior. One thread per (problem, action dim) walks h
+// upwards, so mu_out may alias mu_prev (step h reads h+1 before anything writes it) and
+// sigma_out may alias sigma_prior.
+__global__ void k_warm_start(const float* mu_prev, const float* mu_prior, const float* sigma_prior,
+                             int B, int H, int A, float* mu_out, float* sigma_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * A) return;
+  const int b = i / A, j = i % A;
+  const long long base = (long long)b * H * A + j;
+  for (int h = 0; h + 1 < H; ++h) mu_out[base + (long long)h * A] = mu_prev[base + (long long)(h + 1) * A];
+  mu_out[base + (long long)(H - 1) * A] = mu_prior[base + (long long)(H - 1) * A];
+  for (int h = 0; h < H; ++h) sigma_out[base + (long long)h * A] = sigma_prior[base + (long long)h * A];
+}
+
+cudaError_t warm_start(const float* mu_prev, const float* mu_prior, const float* sigma_prior, int B,
+                       int H, int A, float* mu_out, float* sigma_out, cudaStream_t s) {
+  const int n = B * A;
+  k_warm_start<<<(n + 127) / 128, 128, 0, s>>>(mu_prev, mu_prior, sigma_prior, B, H, A, mu_out,
+                                               sigma_out);
+  return cudaGetLastError();
+}
+
+// State of the next control step, s' = s + a (the same integration the rollout uses
+// between frame blocks). s_out may alias s.
+__global__ void k_state_step(const float* st, const float* a, int n, float* s_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) s_out[i] = st[i] + a[i];
+}
+
+cudaError_t state_step(const float* st, const float* a, int n, float* s_out, cudaStream_t s) {
+  k_state_step<<<(n + 127) / 128, 128, 0, s>>>(st, a, n, s_out);
+  return cudaGetLastError();
+}
+
 __global__ void k_set_u64(uint64_t* p, uint64_t v) { *p = v; }
 
 cudaError_t set_u64(uint64_t* p, uint64_t v, cudaStream_t s) {

@@ -80,6 +80,12 @@ struct jepa_ctx {
   cudaStream_t cap_stream = nullptr;
   bool profile = false;
   PlanGraph* last_plan = nullptr;
+  // closed-loop episode state (grow-only; see jepa_cem_closed_loop)
+  std::vector<void*> ep_allocs;
+  int ep_B = 0, ep_H = 0, ep_R = 0;
+  float *ep_z[2] = {nullptr, nullptr}, *ep_s[2] = {nullptr, nullptr}, *ep_goal = nullptr;
+  float *ep_mu_prior = nullptr, *ep_sg_prior = nullptr, *ep_mu0 = nullptr, *ep_sg0 = nullptr;
+  float *ep_mu_trace = nullptr, *ep_a = nullptr, *ep_dist = nullptr;
   std::map<std::tuple<int, int, int, int, int, bool>, PlanGraph*> graphs;
 };
 
@@ -525,6 +531,7 @@ void jepa_destroy(jepa_ctx* ctx) {
   cudaSetDevice(ctx->device);
   drop_graphs(ctx);
   free_list(ctx->ws_allocs);
+  free_list(ctx->ep_allocs);
   if (ctx->w.f32) cudaFree(ctx->w.f32);
   if (ctx->w.mats) cudaFree(ctx->w.mats);
   if (ctx->fw_base) cudaFree(ctx->fw_base);
@@ -768,6 +775,110 @@ jepa_status jepa_cem_plan(jepa_ctx* ctx, const float* z0, const float* state0, c
       CK(cudaMemcpyAsync(trace->winner, g->winner, (size_t)B * 4, cudaMemcpyDefault, s));
   }
   ctx->last_plan = g;
+  return JEPA_OK;
+}
+
+jepa_status jepa_cem_warm_start(jepa_ctx* ctx, const float* mu_prev, const float* mu_prior,
+                                const float* sigma_prior, int B, int H, float* mu_out,
+                                float* sigma_out, void* stream) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  if (bad_ptr(mu_prev) || bad_ptr(mu_prior) || bad_ptr(sigma_prior) || bad_ptr(mu_out) ||
+      bad_ptr(sigma_out) || B < 1 || H < 1)
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "warm_start: bad argument");
+  if ((long long)B * H * ctx->cfg.action_dim > (1LL << 30))
+    return fail(ctx, JEPA_ERR_SHAPE, "warm_start: too large");
+  CK(cudaSetDevice(ctx->device));
+  CK(warm_start(mu_prev, mu_prior, sigma_prior, B, H, ctx->cfg.action_dim, mu_out, sigma_out,
+                (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
+jepa_status jepa_world_model_step(jepa_ctx* ctx, const float* z, const float* state,
+                                  const float* action, int B, const float* goal, float* z_next,
+                                  float* state_next, float* distance, void* stream) {
+  jepa_status st = check_ready(ctx);
+  if (st) return st;
+  if (bad_ptr(z) || bad_ptr(state) || bad_ptr(action) || bad_ptr(z_next) || bad_ptr(state_next) ||
+      B < 1 || (distance && !goal) || z_next == z)
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "world_model_step: bad argument");
+  // the predicted frame first: it reads `state`, which state_next may overwrite
+  if ((st = jepa_predictor_forward(ctx, z, state, action, B, 1, 1, goal, z_next, distance,
+                                   stream)))
+    return st;
+  CK(state_step(state, action, B * ctx->cfg.state_dim, state_next, (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
+jepa_status jepa_cem_closed_loop(jepa_ctx* ctx, const float* z0, const float* state0,
+                                 const float* goal, const float* mu_prior,
+                                 const float* sigma_prior, int B, int H, int N, int K, int rounds,
+                                 int steps, int warm, uint64_t seed, float* actions_out,
+                                 float* distance_out, void* stream) {
+  jepa_status st = check_ready(ctx);
+  if (st) return st;
+  if (bad_ptr(z0) || bad_ptr(state0) || bad_ptr(goal) || bad_ptr(mu_prior) ||
+      bad_ptr(sigma_prior) || bad_ptr(actions_out) || bad_ptr(distance_out) || steps < 1 ||
+      (warm != 0 && warm != 1))
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "closed_loop: bad argument");
+  if ((st = plan_args(ctx, B, H, N, K, rounds))) return st;
+  const jepa_config& c = ctx->cfg;
+  const size_t PE = (size_t)c.patch_tokens * c.embed_dim, A = c.action_dim, S = c.state_dim;
+  const size_t HA = (size_t)H * A;
+  if (B > ctx->ep_B || H > ctx->ep_H || rounds > ctx->ep_R) {
+    const int nB = B > ctx->ep_B ? B : ctx->ep_B, nH = H > ctx->ep_H ? H : ctx->ep_H;
+    const int nR = rounds > ctx->ep_R ? rounds : ctx->ep_R;
+    CK(cudaDeviceSynchronize());
+    free_list(ctx->ep_allocs);
+    ctx->ep_B = ctx->ep_H = ctx->ep_R = 0;
+    const size_t nHA = (size_t)nH * A;
+    if ((st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_z[0], nB * PE * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_z[1], nB * PE * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_s[0], nB * S * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_s[1], nB * S * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_goal, nB * PE * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_mu_prior, nB * nHA * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_sg_prior, nB * nHA * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_mu0, nB * nHA * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_sg0, nB * nHA * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_mu_trace, (nR + 1) * nB * nHA * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_a, nB * A * 4)) ||
+        (st = dalloc(ctx, ctx->ep_allocs, &ctx->ep_dist, nB * 4))) {
+      free_list(ctx->ep_allocs);
+      return st;
+    }
+    ctx->ep_B = nB;
+    ctx->ep_H = nH;
+    ctx->ep_R = nR;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(cudaMemcpyAsync(ctx->ep_z[0], z0, B * PE * 4, cudaMemcpyDefault, s));
+  CK(cudaMemcpyAsync(ctx->ep_s[0], state0, B * S * 4, cudaMemcpyDefault, s));
+  CK(cudaMemcpyAsync(ctx->ep_goal, goal, B * PE * 4, cudaMemcpyDefault, s));
+  CK(cudaMemcpyAsync(ctx->ep_mu_prior, mu_prior, B * HA * 4, cudaMemcpyDefault, s));
+  CK(cudaMemcpyAsync(ctx->ep_sg_prior, sigma_prior, B * HA * 4, cudaMemcpyDefault, s));
+  jepa_cem_trace tr;
+  memset(&tr, 0, sizeof tr);
+  tr.mu = ctx->ep_mu_trace;
+  for (int t = 0; t < steps; ++t) {
+    const int cur = t & 1, nxt = cur ^ 1;
+    const bool from_prior = t == 0 || !warm;
+    if (!from_prior)
+      CK(warm_start(ctx->ep_mu_trace + (size_t)rounds * B * HA, ctx->ep_mu_prior,
+                    ctx->ep_sg_prior, B, H, (int)A, ctx->ep_mu0, ctx->ep_sg0, s));
+    if ((st = jepa_cem_plan(ctx, ctx->ep_z[cur], ctx->ep_s[cur], ctx->ep_goal,
+                            from_prior ? ctx->ep_mu_prior : ctx->ep_mu0,
+                            from_prior ? ctx->ep_sg_prior : ctx->ep_sg0, B, H, N, K, rounds,
+                            seed + (uint64_t)t, ctx->ep_a, &tr, stream)))
+      return st;
+    if ((st = jepa_world_model_step(ctx, ctx->ep_z[cur], ctx->ep_s[cur], ctx->ep_a, B,
+                                    ctx->ep_goal, ctx->ep_z[nxt], ctx->ep_s[nxt], ctx->ep_dist,
+                                    stream)))
+      return st;
+    CK(cudaMemcpyAsync(actions_out + (size_t)t * B * A, ctx->ep_a, B * A * 4, cudaMemcpyDefault,
+                       s));
+    CK(cudaMemcpyAsync(distance_out + (size_t)t * B, ctx->ep_dist, (size_t)B * 4,
+                       cudaMemcpyDefault, s));
+  }
   return JEPA_OK;
 }
 

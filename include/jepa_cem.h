@@ -159,6 +159,47 @@ jepa_status jepa_cem_plan(jepa_ctx* ctx, const float* z0, const float* state0, c
                           int rounds, uint64_t seed, float* action_out,
                           const jepa_cem_trace* trace, void* stream);
 
+/* Warm start of the next planning step under receding-horizon control (planning page,
+ * section "Further Optimization", B "Warm-started CEM": only the first action of a plan is
+ * executed, and the rest of it may seed the next step instead of a fresh Gaussian).
+ *   mu_prev [B,H,A] dev        the previous plan's last-round mean (the slice
+ *                              trace->mu + rounds*B*H*A of jepa_cem_plan's trace)
+ *   mu_prior, sigma_prior [B,H,A] dev   the fresh Gaussian
+ *   mu_out, sigma_out [B,H,A] dev       outputs; mu_out may equal mu_prev and sigma_out may
+ *                                       equal sigma_prior (no other overlap)
+ * mu_out[b,h] = mu_prev[b,h+1] for h < H-1, mu_out[b,H-1] = mu_prior[b,H-1];
+ * sigma_out = sigma_prior. With H = 1 this is the prior itself. */
+jepa_status jepa_cem_warm_start(jepa_ctx* ctx, const float* mu_prev, const float* mu_prior,
+                                const float* sigma_prior, int B, int H, float* mu_out,
+                                float* sigma_out, void* stream);
+
+/* One step of the world model standing in for the robot (the closed-loop tests of the same
+ * section use the world model as the simulator): the executed action goes through the
+ * predictor with horizon 1.
+ *   z [B,P,E], state [B,S], action [B,A]: dev inputs
+ *   z_next [B,P,E] dev   output: the predicted next frame (must not overlap z)
+ *   state_next [B,S] dev output: state + action (may equal state)
+ *   goal [B,P,E] dev or NULL; distance [B] dev or NULL: mean |z_next - goal| (needs goal) */
+jepa_status jepa_world_model_step(jepa_ctx* ctx, const float* z, const float* state,
+                                  const float* action, int B, const float* goal, float* z_next,
+                                  float* state_next, float* distance, void* stream);
+
+/* Closed-loop episode: `steps` times (plan with jepa_cem_plan, execute the winner's first
+ * action with jepa_world_model_step, replan from the predicted frame), all enqueued on
+ * `stream` with no host synchronisation between steps. Step t plans with seed + t and
+ * starts from the prior (warm = 0) or, for t >= 1, from jepa_cem_warm_start of step t-1's
+ * last-round mean (warm = 1).
+ *   z0, goal [B,P,E], state0 [B,S], mu_prior, sigma_prior [B,H,A]: dev|host inputs
+ *   actions_out [steps,B,A]: dev|host output, the executed actions
+ *   distance_out [steps,B]: dev|host output, mean |z_{t+1} - goal| after each action
+ * Workspace for the episode is kept in the context and grows on demand (the first call
+ * with larger sizes synchronises the device). */
+jepa_status jepa_cem_closed_loop(jepa_ctx* ctx, const float* z0, const float* state0,
+                                 const float* goal, const float* mu_prior,
+                                 const float* sigma_prior, int B, int H, int N, int K, int rounds,
+                                 int steps, int warm, uint64_t seed, float* actions_out,
+                                 float* distance_out, void* stream);
+
 /* Number of kernel launches one jepa_cem_plan call with these sizes makes (captures
  * the graph if needed). */
 jepa_status jepa_plan_kernel_count(jepa_ctx* ctx, int B, int H, int N, int K, int rounds,
