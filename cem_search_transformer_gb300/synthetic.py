@@ -41,6 +41,7 @@ class PredictorConfig:
     state_dim: int = 7   # S
     precision: str = "bf16"  # "fp32" or "bf16"
     ln_eps: float = 1e-5
+    mlp_kind: str = "gelu"   # "gelu": W_2 GELU(W_1 x); "gated": W_2 (W_1 x * GELU(W_g x))
 
     @property
     def tokens(self) -> int:
@@ -72,11 +73,23 @@ SMALL = PredictorConfig("small", layers=6, width=384, heads=6, mlp=1536,
 FULL = PredictorConfig("full", layers=24, width=1024, heads=16, mlp=4096,
                        patch_tokens=256, embed_dim=1408, precision="bf16")
 
+# Gated-MLP variants (the Realtime-VLA notes' FFN: FC1(x) * GELU(FC2(x))) with the same
+# hidden width m as their GELU counterparts.
+TINY_GATED = dataclasses.replace(TINY, name="tiny_gated", mlp_kind="gated")
+SMALL_GATED = dataclasses.replace(SMALL, name="small_gated", mlp_kind="gated")
+FULL_GATED = dataclasses.replace(FULL, name="full_gated", mlp_kind="gated")
+
+PRESETS: Dict[str, PredictorConfig] = {c.name: c for c in (TINY, SMALL, FULL, TINY_GATED,
+                                                            SMALL_GATED, FULL_GATED)}
+
 WORKLOADS: Dict[str, CemConfig] = {
     "tiny": CemConfig(TINY, B=1, N=64, K=8, rounds=2, horizon=1),
     "small": CemConfig(SMALL, B=1, N=200, K=20, rounds=5, horizon=2),
     "full": CemConfig(FULL, B=1, N=800, K=80, rounds=10, horizon=1),
     "multistep": CemConfig(FULL, B=1, N=800, K=80, rounds=10, horizon=3),
+    "tiny_gated": CemConfig(TINY_GATED, B=1, N=64, K=8, rounds=2, horizon=1),
+    "small_gated": CemConfig(SMALL_GATED, B=1, N=200, K=20, rounds=5, horizon=2),
+    "full_gated": CemConfig(FULL_GATED, B=1, N=800, K=80, rounds=10, horizon=1),
 }
 for _n in (100, 200, 400, 800, 1600, 3200):
     for _b in (1, 4, 8):
@@ -89,7 +102,10 @@ def weight_names(cfg: PredictorConfig) -> List[str]:
     names = ["W_in", "b_in", "W_a", "b_a", "W_s", "b_s", "pos"]
     for l in range(cfg.layers):
         names += [f"l{l}.{n}" for n in ("ln1_g", "ln1_b", "W_qkv", "b_qkv", "W_o", "b_o",
-                                         "ln2_g", "ln2_b", "W_1", "b_1", "W_2", "b_2")]
+                                         "ln2_g", "ln2_b", "W_1", "b_1")]
+        if cfg.mlp_kind == "gated":
+            names += [f"l{l}.W_g", f"l{l}.b_g"]
+        names += [f"l{l}.W_2", f"l{l}.b_2"]
     names += ["lnf_g", "lnf_b", "W_out", "b_out"]
     return names
 
@@ -104,6 +120,8 @@ def weight_shapes(cfg: PredictorConfig) -> Dict[str, tuple]:
                        f"l{l}.b_qkv": (3 * d,), f"l{l}.W_o": (d, d), f"l{l}.b_o": (d,),
                        f"l{l}.ln2_g": (d,), f"l{l}.ln2_b": (d,), f"l{l}.W_1": (m, d),
                        f"l{l}.b_1": (m,), f"l{l}.W_2": (d, m), f"l{l}.b_2": (d,)})
+        if cfg.mlp_kind == "gated":
+            shapes.update({f"l{l}.W_g": (m, d), f"l{l}.b_g": (m,)})
     shapes.update({"lnf_g": (d,), "lnf_b": (d,), "W_out": (E, d), "b_out": (E,)})
     return shapes
 

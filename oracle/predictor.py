@@ -17,6 +17,9 @@ rest is the plainest reading, stated here:
   * z_0 = the encoded context frame, z_k = the prediction for k >= 1 (autoregressive);
   * L pre-LN layers: x += W_o Attn(LN1 x) + b_o ; x += W_2 GELU(W_1 LN2 x + b_1) + b_2,
     GELU with erf, LayerNorm eps 1e-5, attention scale 1/sqrt(d/h);
+  * gated-MLP variant (the Realtime-VLA notes, section 4.2 "Fusing Gated Linear Layers":
+    the up-projection is FC1(x, w1) * GELU(FC2(x, w2))): with FC1 = W_1, b_1 and
+    FC2 = W_g, b_g, x += W_2 [(W_1 h + b_1) * GELU(W_g h + b_g)] + b_2, h = LN2 x;
   * block-causal mask: a query in block i sees every key of blocks j <= i;
   * prediction z_{k+1}[p] = W_out LN_f(x at patch p of block k) + b_out;
   * energy = mean over the P x E entries of |z_H - goal| (L1; the mean ranks like the sum).
@@ -24,8 +27,8 @@ rest is the plainest reading, stated here:
 Each rollout step is a full recompute over blocks 0..k with the mask. That is the
 definition; a KV cache reaches the same values because of block causality.
 
-In bf16 mode the six matrices that the CUDA path stores in bf16 (W_in, W_qkv, W_o,
-W_1, W_2, W_out) are rounded to bf16 (round to nearest even) before upcasting; all
+In bf16 mode the matrices that the CUDA path stores in bf16 (W_in, W_qkv, W_o, W_1,
+W_g, W_2, W_out) are rounded to bf16 (round to nearest even) before upcasting; all
 activations stay float64.
 """
 from __future__ import annotations
@@ -35,7 +38,7 @@ from typing import Dict, List
 import numpy as np
 from scipy.special import erf
 
-MATRIX_SUFFIXES = ("W_in", "W_qkv", "W_o", "W_1", "W_2", "W_out")
+MATRIX_SUFFIXES = ("W_in", "W_qkv", "W_o", "W_1", "W_g", "W_2", "W_out")
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -98,7 +101,11 @@ def transformer_layer(x: np.ndarray, w: Dict[str, np.ndarray], l: int, heads: in
     o = attention(q, k, v, allowed).transpose(0, 2, 1, 3).reshape(n, L, d)
     x = x + o @ w[f"l{l}.W_o"].T + w[f"l{l}.b_o"]
     h2 = layer_norm(x, w[f"l{l}.ln2_g"], w[f"l{l}.ln2_b"], eps)
-    u = gelu(h2 @ w[f"l{l}.W_1"].T + w[f"l{l}.b_1"])
+    fc1 = h2 @ w[f"l{l}.W_1"].T + w[f"l{l}.b_1"]
+    if f"l{l}.W_g" in w:                                  # gated MLP
+        u = fc1 * gelu(h2 @ w[f"l{l}.W_g"].T + w[f"l{l}.b_g"])
+    else:
+        u = gelu(fc1)
     return x + u @ w[f"l{l}.W_2"].T + w[f"l{l}.b_2"]
 
 

@@ -106,6 +106,79 @@ def test_layer_matches_torch_encoder_layer():
     assert np.allclose(got, ref, rtol=1e-10, atol=1e-11)
 
 
+def _torch_layer(w, l, cfg, W1, b1, activation):
+    """torch.nn.TransformerEncoderLayer (pre-LN) carrying layer l's weights, with the given
+    first MLP linear and activation."""
+    layer = torch.nn.TransformerEncoderLayer(cfg.width, cfg.heads, cfg.mlp, dropout=0.0,
+                                             activation=activation, layer_norm_eps=cfg.ln_eps,
+                                             batch_first=True, norm_first=True,
+                                             dtype=torch.float64)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    with torch.no_grad():
+        layer.self_attn.in_proj_weight.copy_(t(w[f"l{l}.W_qkv"]))
+        layer.self_attn.in_proj_bias.copy_(t(w[f"l{l}.b_qkv"]))
+        layer.self_attn.out_proj.weight.copy_(t(w[f"l{l}.W_o"]))
+        layer.self_attn.out_proj.bias.copy_(t(w[f"l{l}.b_o"]))
+        layer.linear1.weight.copy_(t(W1))
+        layer.linear1.bias.copy_(t(b1))
+        layer.linear2.weight.copy_(t(w[f"l{l}.W_2"]))
+        layer.linear2.bias.copy_(t(w[f"l{l}.b_2"]))
+        layer.norm1.weight.copy_(t(w[f"l{l}.ln1_g"]))
+        layer.norm1.bias.copy_(t(w[f"l{l}.ln1_b"]))
+        layer.norm2.weight.copy_(t(w[f"l{l}.ln2_g"]))
+        layer.norm2.bias.copy_(t(w[f"l{l}.ln2_b"]))
+    return layer
+
+
+def test_gated_layer_reduces_to_torch_layers():
+    """Gated MLP u = (W_1 h + b_1) * GELU(W_g h + b_g), pinned by its two degenerate cases:
+    a constant-one linear branch (W_1 = 0, b_1 = 1) leaves a GELU MLP whose first linear is
+    the gate (torch's gelu layer), and a constant gate (W_g = 0, b_g = c) leaves a linear MLP
+    scaled by GELU(c) (torch's layer with that activation). Applying GELU to the wrong branch,
+    dropping a bias or adding instead of multiplying fails one of them."""
+    cfg = dataclasses.replace(MICRO, mlp_kind="gated")
+    w = _w(cfg, seed=8)
+    d, T, nb, l = cfg.width, cfg.tokens, 2, 1
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((2, nb * T, d))
+    allowed = predictor.block_causal_allowed(nb, T)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+
+    w1 = dict(w)
+    w1[f"l{l}.W_1"] = np.zeros_like(w[f"l{l}.W_1"])
+    w1[f"l{l}.b_1"] = np.ones_like(w[f"l{l}.b_1"])
+    got = predictor.transformer_layer(x, w1, l, cfg.heads, allowed, cfg.ln_eps)
+    layer = _torch_layer(w, l, cfg, w[f"l{l}.W_g"], w[f"l{l}.b_g"], "gelu")
+    with torch.no_grad():
+        ref = layer(t(x), src_mask=t(~allowed)).numpy()
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-11)
+
+    c = 1.3
+    w2 = dict(w)
+    w2[f"l{l}.W_g"] = np.zeros_like(w[f"l{l}.W_g"])
+    w2[f"l{l}.b_g"] = np.full_like(w[f"l{l}.b_g"], c)
+    got = predictor.transformer_layer(x, w2, l, cfg.heads, allowed, cfg.ln_eps)
+    g_c = torch.nn.functional.gelu(torch.tensor(c, dtype=torch.float64))
+    layer = _torch_layer(w, l, cfg, w[f"l{l}.W_1"], w[f"l{l}.b_1"], lambda u: u * g_c)
+    with torch.no_grad():
+        ref = layer(t(x), src_mask=t(~allowed)).numpy()
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-11)
+
+    # and the general case differs from both (the gate really multiplies)
+    full = predictor.transformer_layer(x, w, l, cfg.heads, allowed, cfg.ln_eps)
+    assert not np.allclose(full, got, rtol=1e-6)
+
+
+def test_gated_weights_in_canonical_order():
+    cfg = dataclasses.replace(MICRO, mlp_kind="gated")
+    names = synthetic.weight_names(cfg)
+    i = names.index("l0.b_1")
+    assert names[i + 1:i + 5] == ["l0.W_g", "l0.b_g", "l0.W_2", "l0.b_2"]
+    assert synthetic.weight_shapes(cfg)["l0.W_g"] == (cfg.mlp, cfg.width)
+    wb = predictor.prepare_weights(synthetic.make_weights(cfg), "bf16")
+    assert np.array_equal(wb["l0.W_g"], predictor.round_to_bf16(synthetic.make_weights(cfg)["l0.W_g"]))
+
+
 def _incremental_rollout(w, cfg, z0, s0, actions):
     """Independent KV-cached rollout: each layer attends over cached keys/values of earlier blocks."""
     n, H, _ = actions.shape
