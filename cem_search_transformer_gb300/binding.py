@@ -42,7 +42,9 @@ class Config(ctypes.Structure):
                 ("embed_dim", ctypes.c_int32), ("action_dim", ctypes.c_int32),
                 ("state_dim", ctypes.c_int32), ("max_horizon", ctypes.c_int32),
                 ("precision", ctypes.c_int32), ("ln_eps", ctypes.c_float),
-                ("max_chunk", ctypes.c_int32)]
+                ("max_chunk", ctypes.c_int32), ("mlp_kind", ctypes.c_int32)]
+
+MLP_KINDS = {"gelu": 0, "gated": 1}
 
 
 class Trace(ctypes.Structure):
@@ -95,13 +97,14 @@ def load(path: str = _LIB_PATH):
 def make_config(pc: synthetic.PredictorConfig, max_horizon: int = 1, max_chunk: int = 0) -> Config:
     return Config(pc.layers, pc.width, pc.heads, pc.mlp, pc.patch_tokens, pc.embed_dim,
                   pc.action_dim, pc.state_dim, max_horizon, 1 if pc.precision == "bf16" else 0,
-                  pc.ln_eps, max_chunk)
+                  pc.ln_eps, max_chunk, MLP_KINDS[pc.mlp_kind])
 
 
 def pack_weights(pc: synthetic.PredictorConfig, weights: Dict[str, np.ndarray]) -> bytes:
     """Weight blob: 64-byte header + fp32 tensors in canonical order (format only)."""
-    hdr = struct.pack("<10i", 0x4150454A, 1, pc.layers, pc.width, pc.heads, pc.mlp,
-                      pc.patch_tokens, pc.embed_dim, pc.action_dim, pc.state_dim).ljust(64, b"\0")
+    hdr = struct.pack("<11i", 0x4150454A, 1, pc.layers, pc.width, pc.heads, pc.mlp,
+                      pc.patch_tokens, pc.embed_dim, pc.action_dim, pc.state_dim,
+                      MLP_KINDS[pc.mlp_kind]).ljust(64, b"\0")
     shapes = synthetic.weight_shapes(pc)
     parts = [hdr]
     for name in synthetic.weight_names(pc):

@@ -28,6 +28,10 @@ enum EpiMode : int {
   EPI_RESID = 2,    // x  += acc + bias   (fp32 residual)    (attention out-proj, MLP down)
   EPI_INPROJ = 3,   // x   = acc + bias + pos[token]         (patch in-projection)
   EPI_OUTPROJ = 4,  // z = acc + bias; optional z outputs; optional L1 energy partials
+  EPI_GATED = 5,    // gated MLP up: W rows hold FC1 and gate blocks of 32 interleaved
+                    // (block 2p = FC1 rows 32p.., block 2p+1 = gate rows 32p..); output
+                    // column 32p + c = (acc[64p + c] + bias) * gelu(acc[64p + 32 + c] + bias)
+                    // of width N / 2, written to out0 (row stride ld0)
 };
 
 // What a GEMM does with its fp32 accumulators. One struct serves every mode; unused

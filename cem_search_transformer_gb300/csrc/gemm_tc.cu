@@ -35,7 +35,9 @@ constexpr int BM = 128, BK = 64;
 constexpr int STG_FLOATS = 32 * 32;                     // per-warp transpose buffer
 
 // Epilogue warps per CTA for an epilogue mode, and the CTA size (producer + MMA warps too).
-__host__ __device__ constexpr int epi_warps(int mode) { return mode == EPI_GELU ? 16 : 8; }
+__host__ __device__ constexpr int epi_warps(int mode) {
+  return (mode == EPI_GELU || mode == EPI_GATED) ? 16 : 8;
+}
 __host__ __device__ constexpr int cta_threads(int mode) { return 64 + 32 * epi_warps(mode); }
 
 template <int BN, int EW>
@@ -74,12 +76,96 @@ struct Cfg2 {
 // tile n_blk), executed by every epilogue warp. Waits for `tfull` (parity), releases the
 // accumulator through `release(tempty)` as soon as its last TMEM load has landed, then
 // finishes the global stores. Returns false if a bounded wait expired.
+
+// Gated-MLP epilogue (EPI_GATED, 256-column tiles, 16 epilogue warps): each warp owns a
+// 32-row quarter and 64 accumulator columns, i.e. exactly one FC1 block and the gate block
+// that follows it in the interleaved weight. Per half of 16 columns the lane loads its row's
+// FC1 and gate values from TMEM, forms (fc1 + b) * gelu(gate + b) in place, and the 32 outputs
+// of the row go through the warp's staging buffer so that stores are row-contiguous.
+template <int EW, typename Release>
+__device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, int N, int m0,
+                                                    int n_blk, uint32_t tmem_acc, uint32_t tfull,
+                                                    uint32_t tfull_parity, uint32_t tempty,
+                                                    Release release, float* stg, int ew, int warp,
+                                                    int lane, volatile int* abort_flag,
+                                                    int* err_flag) {
+  static_assert(EW == 16, "one FC1/gate block pair per epilogue warp");
+  const int quarter = warp & 3;
+  const int part = ew >> 2;                  // block pair within the 256-column tile
+  const int cbase = n_blk * 256 + part * 64; // FC1 block; the gate block is cbase + 32
+  const int ocol = (cbase >> 1);             // first output column of this pair
+  const bool active = cbase < N;
+  if (!mbar_wait(tfull, tfull_parity, abort_flag, err_flag)) return false;
+  tc_fence_after();
+  const uint32_t tbase = tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * 64);
+  uint32_t r[32];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    if (active) {
+      tmem_ld16_async(tbase + 16u * half, r);
+      tmem_ld16_async(tbase + 32u + 16u * half, r + 16);
+    }
+    tmem_wait(r);
+    if (half == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release(tempty);
+    }
+    if (!active) continue;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = cbase + 16 * half + 4 * k;
+      const float4 b1 = __ldg(reinterpret_cast<const float4*>(epi.bias + c));
+      const float4 bg = __ldg(reinterpret_cast<const float4*>(epi.bias + c + 32));
+      float4 g = make_float4(__uint_as_float(r[16 + 4 * k]) + bg.x,
+                             __uint_as_float(r[16 + 4 * k + 1]) + bg.y,
+                             __uint_as_float(r[16 + 4 * k + 2]) + bg.z,
+                             __uint_as_float(r[16 + 4 * k + 3]) + bg.w);
+      g = gelu4(g);
+      const float4 h = make_float4((__uint_as_float(r[4 * k]) + b1.x) * g.x,
+                                   (__uint_as_float(r[4 * k + 1]) + b1.y) * g.y,
+                                   (__uint_as_float(r[4 * k + 2]) + b1.z) * g.z,
+                                   (__uint_as_float(r[4 * k + 3]) + b1.w) * g.w);
+      const int q = 4 * half + k;            // float4 group of the row's 32 outputs
+      *reinterpret_cast<float4*>(stg + lane * 32 + ((q ^ (lane & 7)) << 2)) = h;
+    }
+  }
+  if (!active) return true;
+  __syncwarp();
+  const int cg = lane & 7, rsub = lane >> 3;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = rsub + 4 * i;
+    const int row = m0 + quarter * 32 + rr;
+    const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
+    if (row >= M) continue;
+    const long long off = map_row(epi.map0, row) * epi.ld0 + ocol + 4 * cg;
+    if (epi.act_bf16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(epi.out0) + off) = u;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(epi.out0) + off) = v;
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
 template <int BN, int MODE, int EW, typename Release>
 __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N, int m0, int n_blk,
                                               uint32_t tmem_acc, uint32_t tfull,
                                               uint32_t tfull_parity, uint32_t tempty,
                                               Release release, float* stg, int ew, int warp,
                                               int lane, volatile int* abort_flag, int* err_flag) {
+  if constexpr (MODE == EPI_GATED) {
+    static_assert(BN == 256, "gated tiles hold four FC1/gate block pairs");
+    return epilogue_tile_gated<EW>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity, tempty,
+                                   release, stg, ew, warp, lane, abort_flag, err_flag);
+  } else {
   const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
   const int part = ew >> 2;                  // which share of the tile's columns
   constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp
@@ -226,6 +312,7 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
     }
   }
   return true;
+  }
 }
 
 template <int BN, int MODE>
@@ -563,6 +650,20 @@ static cudaError_t launch_mode(const bf16* A, const bf16* W, int M, int N, int K
   return cudaErrorInvalidValue;
 }
 
+template <>
+cudaError_t launch_mode<256>(const bf16* A, const bf16* W, int M, int N, int K,
+                             const Epilogue& epi, int* err_flag, int num_sms, cudaStream_t s) {
+  switch (epi.mode) {
+    case EPI_STORE: return launch_tc<256, EPI_STORE>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_GELU: return launch_tc<256, EPI_GELU>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_RESID: return launch_tc<256, EPI_RESID>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_INPROJ: return launch_tc<256, EPI_INPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_OUTPROJ: return launch_tc<256, EPI_OUTPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_GATED: return launch_tc<256, EPI_GATED>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <int MODE>
 static cudaError_t launch_tc2(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                               int* err_flag, int num_sms, cudaStream_t s) {
@@ -589,6 +690,7 @@ cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, cons
   if (K <= 0 || K % 8 != 0 || N % 4 != 0 || (((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
     return cudaErrorInvalidValue;
   if (epi.mode == EPI_STORE && (epi.split % 32) != 0) return cudaErrorInvalidValue;
+  if (epi.mode == EPI_GATED && (N % 256 != 0 || !epi.bias)) return cudaErrorInvalidValue;
   // QKV and the residual projections (N a multiple of 256, many row tiles) run on CTA
   // pairs; the GELU layer keeps single CTAs, whose 16 epilogue warps need the registers
   if (N % 256 == 0 && M >= 4 * BM && num_sms >= 2) {

@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ A,
                                                    int K, Epilogue epi) {
   __shared__ float As[SG_BK][SG_BM + 4];
   __shared__ float Ws[SG_BK][SG_BN + 4];
-  __shared__ float red[SG_BM][17];
+  __shared__ float red[SG_BM][SG_BN / 2 + 1];   // energy partials; gated: gelu(gate) tile
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int m0 = blockIdx.y * SG_BM, n0 = blockIdx.x * SG_BN;
   float acc[4][4] = {};
@@ -427,6 +427,40 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ A,
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], w[j], acc[i][j]);
     }
     __syncthreads();
+  }
+  if (epi.mode == EPI_GATED) {
+    // a 64-column tile is one FC1 block (threads tx < 8) and its gate block (tx >= 8):
+    // the gate threads publish gelu(gate + b), the FC1 threads multiply and store
+    float (*gate)[SG_BN / 2 + 1] = red;
+    if (tx >= 8) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int col = n0 + tx * 4 + j;
+          gate[ty * 4 + i][(tx - 8) * 4 + j] = col < N ? gelu_erf(acc[i][j] + epi.bias[col]) : 0.f;
+        }
+    }
+    __syncthreads();
+    if (tx < 8) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = m0 + ty * 4 + i;
+        if (r >= M) continue;
+        const long long off = map_row(epi.map0, r) * epi.ld0 + (n0 >> 1) + tx * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int col = n0 + tx * 4 + j;
+          if (col >= N) continue;
+          const float h = (acc[i][j] + epi.bias[col]) * gate[ty * 4 + i][tx * 4 + j];
+          if (epi.act_bf16)
+            reinterpret_cast<bf16*>(epi.out0)[off + j] = __float2bfloat16_rn(h);
+          else
+            reinterpret_cast<float*>(epi.out0)[off + j] = h;
+        }
+      }
+    }
+    return;
   }
   const int c = n0 + tx * 4;
 #pragma unroll
@@ -454,6 +488,7 @@ int gemm_simt_partials(int N) { return (N + SG_BN - 1) / SG_BN; }
 cudaError_t gemm_simt_f32(const float* A, const float* W, int M, int N, int K, const Epilogue& epi,
                           cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
+  if (epi.mode == EPI_GATED && (N % SG_BN != 0 || !epi.bias)) return cudaErrorInvalidValue;
   dim3 grid((N + SG_BN - 1) / SG_BN, (M + SG_BM - 1) / SG_BM);
   k_gemm_simt<<<grid, 256, 0, s>>>(A, W, M, N, K, epi);
   return cudaGetLastError();

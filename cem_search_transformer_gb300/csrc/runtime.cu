@@ -30,11 +30,14 @@ constexpr int kMaxSelectN = 8192;
 struct LayerW {
   const float *ln1_g, *ln1_b, *b_qkv, *b_o, *ln2_g, *ln2_b, *b_1, *b_2;
   const void *W_qkv, *W_o, *W_1, *W_2;  // bf16 (bf16 mode) or fp32
+  // gated MLP: W_1 and b_1 above point at the interleaved [FC1 | gate] pair (2m rows)
 };
 
 struct Weights {
   float* f32 = nullptr;   // device copy of every tensor (blob minus header)
   bf16* mats = nullptr;   // bf16 copies of the GEMM matrices (bf16 mode)
+  void* gmat = nullptr;   // gated MLP: per layer W_1 / W_g rows interleaved in blocks of 32
+  float* gbias = nullptr; // gated MLP: per layer b_1 / b_g interleaved the same way
   const float *b_in, *W_a, *b_a, *W_s, *b_s, *pos, *lnf_g, *lnf_b, *b_out;
   const void *W_in, *W_out;
   std::vector<LayerW> layers;
@@ -118,6 +121,7 @@ size_t blob_floats(const jepa_config* c) {
                T = c->patch_tokens + 2;
   size_t n = d * E + d + d * A + d + d * S + d + T * d;
   n += (size_t)c->layers * (2 * d + 3 * d * d + 3 * d + d * d + d + 2 * d + m * d + m + d * m + d);
+  if (c->mlp_kind == JEPA_MLP_GATED) n += (size_t)c->layers * (m * d + m);
   n += 2 * d + E * d + E;
   return n;
 }
@@ -128,11 +132,13 @@ jepa_status validate_config(const jepa_config* c) {
       c->embed_dim < 32 || c->action_dim < 1 || c->action_dim > 32 || c->state_dim != c->action_dim ||
       c->max_horizon < 1 || c->max_horizon > 16 || c->width % c->heads != 0 || c->width % 32 ||
       c->embed_dim % 32 || c->mlp % 32 || c->width > 2048 || !(c->ln_eps >= 0.f) ||
-      c->max_chunk < 0 || c->max_chunk > 65535)
+      c->max_chunk < 0 || c->max_chunk > 65535 ||
+      (c->mlp_kind != JEPA_MLP_GELU && c->mlp_kind != JEPA_MLP_GATED))
     return JEPA_ERR_SHAPE;
   const int hd = c->width / c->heads;
   if (c->precision == JEPA_BF16) {
     if (hd != 64 || c->width % 64 || c->embed_dim % 64 || c->mlp % 64) return JEPA_ERR_SHAPE;
+    if (c->mlp_kind == JEPA_MLP_GATED && c->mlp % 128) return JEPA_ERR_SHAPE;
   } else if (c->precision == JEPA_FP32) {
     if (hd % 32 || hd > 128) return JEPA_ERR_SHAPE;
   } else {
@@ -337,11 +343,12 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
         CK(layernorm(ctx->x, identity_map(), ctx->xn, bf16_mode(ctx), lw.ln2_g, lw.ln2_b, rows, d,
                      c.ln_eps, s));
         {
-          Epilogue e = epi_base(ctx, EPI_GELU);
+          const bool gated = c.mlp_kind == JEPA_MLP_GATED;
+          Epilogue e = epi_base(ctx, gated ? EPI_GATED : EPI_GELU);
           e.bias = lw.b_1;
           e.out0 = ctx->hbuf;
           e.ld0 = m;
-          if ((st = gemm(ctx, ctx->xn, lw.W_1, rows, m, d, e, s, prof))) return st;
+          if ((st = gemm(ctx, ctx->xn, lw.W_1, rows, gated ? 2 * m : m, d, e, s, prof))) return st;
         }
         {
           Epilogue e = epi_base(ctx, EPI_RESID);
@@ -534,6 +541,8 @@ void jepa_destroy(jepa_ctx* ctx) {
   free_list(ctx->ep_allocs);
   if (ctx->w.f32) cudaFree(ctx->w.f32);
   if (ctx->w.mats) cudaFree(ctx->w.mats);
+  if (ctx->w.gmat) cudaFree(ctx->w.gmat);
+  if (ctx->w.gbias) cudaFree(ctx->w.gbias);
   if (ctx->fw_base) cudaFree(ctx->fw_base);
   if (ctx->fw_z) cudaFree(ctx->fw_z);
   if (ctx->dev_err) cudaFree(ctx->dev_err);
@@ -553,9 +562,9 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
                 kHeaderBytes + nf * 4);
   int32_t hdr[16];
   memcpy(hdr, host_blob, sizeof hdr);
-  const int32_t want[10] = {kMagic, 1, c.layers, c.width, c.heads, c.mlp, c.patch_tokens,
-                            c.embed_dim, c.action_dim, c.state_dim};
-  for (int i = 0; i < 10; ++i)
+  const int32_t want[11] = {kMagic, 1, c.layers, c.width, c.heads, c.mlp, c.patch_tokens,
+                            c.embed_dim, c.action_dim, c.state_dim, c.mlp_kind};
+  for (int i = 0; i < 11; ++i)
     if (hdr[i] != want[i])
       return fail(ctx, JEPA_ERR_SHAPE, "blob header field %d is %d, expected %d", i, hdr[i], want[i]);
   const float* src = (const float*)((const uint8_t*)host_blob + kHeaderBytes);
@@ -589,7 +598,9 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
   w.W_s = take(d * S);
   w.b_s = take(d);
   w.pos = take(T * d);
+  const bool gated = c.mlp_kind == JEPA_MLP_GATED;
   std::vector<const float*> lm;  // per layer: W_qkv, W_o, W_1, W_2 (fp32)
+  std::vector<const float*> g_w1, g_b1, g_wg, g_bg;  // gated: the two branches, fp32
   for (int l = 0; l < c.layers; ++l) {
     LayerW L;
     L.ln1_g = take(d);
@@ -600,8 +611,17 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
     L.b_o = take(d);
     L.ln2_g = take(d);
     L.ln2_b = take(d);
-    lm.push_back(take_mat(m * d));
-    L.b_1 = take(m);
+    if (gated) {
+      lm.push_back(take(m * d));
+      L.b_1 = take(m);
+      g_w1.push_back(lm.back());
+      g_b1.push_back(L.b_1);
+      g_wg.push_back(take(m * d));
+      g_bg.push_back(take(m));
+    } else {
+      lm.push_back(take_mat(m * d));
+      L.b_1 = take(m);
+    }
     lm.push_back(take_mat(d * m));
     L.b_2 = take(d);
     w.layers.push_back(L);
@@ -640,7 +660,7 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
     for (int l = 0; l < c.layers; ++l) {
       w.layers[l].W_qkv = conv[(size_t)(lm[4 * l] - f32)];
       w.layers[l].W_o = conv[(size_t)(lm[4 * l + 1] - f32)];
-      w.layers[l].W_1 = conv[(size_t)(lm[4 * l + 2] - f32)];
+      if (!gated) w.layers[l].W_1 = conv[(size_t)(lm[4 * l + 2] - f32)];
       w.layers[l].W_2 = conv[(size_t)(lm[4 * l + 3] - f32)];
     }
   } else {
@@ -653,9 +673,51 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
       w.layers[l].W_2 = lm[4 * l + 3];
     }
   }
+  if (gated) {
+    // one up-projection GEMM per layer over [FC1 | gate] rows interleaved in blocks of 32
+    // (2-D copies on the device), converted to bf16 in bf16 mode
+    const size_t nmat = 2 * m * d, nb = 2 * m;
+    float* tmp = nullptr;
+    e = cudaMalloc(&w.gbias, c.layers * nb * 4);
+    if (e == cudaSuccess) e = cudaMalloc(&w.gmat, c.layers * nmat * (bf16_mode(ctx) ? 2 : 4));
+    if (e == cudaSuccess && bf16_mode(ctx)) e = cudaMalloc(&tmp, nmat * 4);
+    for (int l = 0; l < c.layers && e == cudaSuccess; ++l) {
+      float* dm = bf16_mode(ctx) ? tmp : (float*)w.gmat + l * nmat;
+      float* db = w.gbias + l * nb;
+      const size_t row = d * 4;
+      e = cudaMemcpy2D(dm, 64 * row, g_w1[l], 32 * row, 32 * row, m / 32, cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2D(dm + 32 * d, 64 * row, g_wg[l], 32 * row, 32 * row, m / 32,
+                         cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2D(db, 64 * 4, g_b1[l], 32 * 4, 32 * 4, m / 32, cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2D(db + 32, 64 * 4, g_bg[l], 32 * 4, 32 * 4, m / 32,
+                         cudaMemcpyDeviceToDevice);
+      if (e == cudaSuccess && bf16_mode(ctx))
+        e = convert_f32_bf16(tmp, (bf16*)w.gmat + l * nmat, (long long)nmat, 0);
+      if (e == cudaSuccess && bf16_mode(ctx)) e = cudaDeviceSynchronize();  // tmp is reused
+      if (e == cudaSuccess) {
+        w.layers[l].W_1 = bf16_mode(ctx) ? (const void*)((bf16*)w.gmat + l * nmat)
+                                         : (const void*)((float*)w.gmat + l * nmat);
+        w.layers[l].b_1 = db;
+      }
+    }
+    if (tmp) cudaFree(tmp);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(f32);
+      if (w.mats) cudaFree(w.mats);
+      if (w.gmat) cudaFree(w.gmat);
+      if (w.gbias) cudaFree(w.gbias);
+      return fail(ctx, JEPA_ERR_CUDA, "gated MLP weights: %s", cudaGetErrorString(e));
+    }
+  }
   drop_graphs(ctx);  // captured graphs hold the old weight pointers
   if (ctx->w.f32) cudaFree(ctx->w.f32);
   if (ctx->w.mats) cudaFree(ctx->w.mats);
+  if (ctx->w.gmat) cudaFree(ctx->w.gmat);
+  if (ctx->w.gbias) cudaFree(ctx->w.gbias);
   ctx->w = w;
   ctx->loaded = true;
   return JEPA_OK;
@@ -903,12 +965,14 @@ jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W
     return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_bf16: bad argument");
   if ((((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
     return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_bf16: A and W must be 16-byte aligned");
+  if (gelu < 0 || gelu > 2 || (gelu == 2 && (N % 256 != 0 || !bias)))
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_bf16: gated mode needs N %% 256 == 0 and a bias");
   CK(cudaSetDevice(ctx->device));
-  Epilogue e = epi_base(ctx, gelu ? EPI_GELU : EPI_STORE);
+  Epilogue e = epi_base(ctx, gelu == 2 ? EPI_GATED : gelu ? EPI_GELU : EPI_STORE);
   e.act_bf16 = 0;
   e.bias = bias;
   e.out0 = out;
-  e.ld0 = N;
+  e.ld0 = gelu == 2 ? N / 2 : N;
   CK(gemm_tc_bf16((const bf16*)A, (const bf16*)W, M, N, K, e, ctx->dev_err, ctx->num_sms,
                   (cudaStream_t)stream));
   return JEPA_OK;

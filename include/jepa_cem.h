@@ -52,13 +52,19 @@ typedef enum {
 
 typedef enum { JEPA_FP32 = 0, JEPA_BF16 = 1 } jepa_precision;
 
+/* MLP of each layer. GELU: u = GELU(W_1 h + b_1). GATED (the Realtime-VLA notes, section 4.2
+ * "Fusing Gated Linear Layers": FC1(x, w1) * GELU(FC2(x, w2))): u = (W_1 h + b_1) *
+ * GELU(W_g h + b_g), computed by one GEMM over the two weight matrices' rows interleaved in
+ * blocks of 32, whose epilogue writes only the product. */
+typedef enum { JEPA_MLP_GELU = 0, JEPA_MLP_GATED = 1 } jepa_mlp_kind;
+
 /* Predictor shape. Pre-LN transformer, block-causal over frame blocks of
  * T = patch_tokens + 2 tokens ([action, state, P patches]). */
 typedef struct {
   int32_t layers;        /* L */
   int32_t width;         /* d, multiple of 32 (bf16: multiple of 64) */
   int32_t heads;         /* h; head dim d/h = 64 in bf16 mode, <= 128 in fp32 mode */
-  int32_t mlp;           /* m, hidden width of the GELU MLP */
+  int32_t mlp;           /* m, hidden width of the MLP (bf16 gated: multiple of 128) */
   int32_t patch_tokens;  /* P */
   int32_t embed_dim;     /* E, multiple of 32 (bf16: multiple of 64) */
   int32_t action_dim;    /* A (7 in the planning workloads) */
@@ -67,6 +73,7 @@ typedef struct {
   int32_t precision;     /* jepa_precision: FP32 = SIMT fp32 path, BF16 = tensor-core path */
   float ln_eps;          /* LayerNorm epsilon (1e-5) */
   int32_t max_chunk;     /* candidates per predictor pass (0 = library default); bounds workspace */
+  int32_t mlp_kind;      /* jepa_mlp_kind */
 } jepa_config;
 
 typedef struct jepa_ctx jepa_ctx;
@@ -96,10 +103,11 @@ const char* jepa_status_string(jepa_status s);
 
 /* Size in bytes of the weight blob for *cfg: a 64-byte header (int32 magic 0x4150454A,
  * version 1, layers, width, heads, mlp, patch_tokens, embed_dim, action_dim, state_dim,
- * then zeros) followed by float32 tensors in this order, each row-major [out, in]:
+ * mlp_kind, then zeros) followed by float32 tensors in this order, each row-major [out, in]:
  * W_in[d,E] b_in[d] W_a[d,A] b_a[d] W_s[d,S] b_s[d] pos[T,d], per layer
  * {ln1_g[d] ln1_b[d] W_qkv[3d,d] b_qkv[3d] W_o[d,d] b_o[d] ln2_g[d] ln2_b[d]
- *  W_1[m,d] b_1[m] W_2[d,m] b_2[d]}, lnf_g[d] lnf_b[d] W_out[E,d] b_out[E]. */
+ *  W_1[m,d] b_1[m] (gated only: W_g[m,d] b_g[m]) W_2[d,m] b_2[d]},
+ * lnf_g[d] lnf_b[d] W_out[E,d] b_out[E]. */
 size_t jepa_weight_blob_bytes(const jepa_config* cfg);
 
 /* Upload predictor weights from a host blob (format above). Validates the header
@@ -208,7 +216,11 @@ jepa_status jepa_plan_kernel_count(jepa_ctx* ctx, int B, int H, int N, int K, in
 /* Dense linear layer on the tensor-core GEMM used by the predictor (bf16 in, fp32
  * accumulate): out[M,N] = act(A[M,K] * W[N,K]^T + bias[N]).
  *   A, W: bf16 bit patterns (uint16) dev; bias [N] dev or NULL; out [M,N] float32 dev.
- *   gelu: 0 = identity, 1 = erf GELU. K a multiple of 8. Needs a bf16 context. */
+ *   gelu: 0 = identity, 1 = erf GELU, 2 = gated: W's rows are FC1 and gate blocks of 32
+ *   interleaved (rows 64p..64p+31 = FC1 rows 32p.., rows 64p+32..64p+63 = gate rows 32p..),
+ *   bias interleaved the same way (required), N a multiple of 256, and
+ *   out[M,N/2][32p + c] = (acc[64p + c] + bias) * GELU(acc[64p + 32 + c] + bias).
+ * K a multiple of 8. Needs a bf16 context. */
 jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W,
                              const float* bias, int M, int N, int K, int gelu, float* out,
                              void* stream);

@@ -28,20 +28,18 @@ def host(t):
 
 @functools.lru_cache(maxsize=4)
 def weights_for(name: str):
-    pc = {"tiny": synthetic.TINY, "small": synthetic.SMALL, "full": synthetic.FULL}[name]
-    return synthetic.make_weights(pc, seed=0)
+    return synthetic.make_weights(synthetic.PRESETS[name], seed=0)
 
 
 @functools.lru_cache(maxsize=4)
 def oracle_weights_for(name: str):
     from oracle import predictor
-    pc = {"tiny": synthetic.TINY, "small": synthetic.SMALL, "full": synthetic.FULL}[name]
-    return predictor.prepare_weights(weights_for(name), pc.precision)
+    return predictor.prepare_weights(weights_for(name), synthetic.PRESETS[name].precision)
 
 
 def make_planner(name: str, max_horizon: int = 1, max_chunk: int = 0):
     from cem_search_transformer_gb300 import binding
-    pc = {"tiny": synthetic.TINY, "small": synthetic.SMALL, "full": synthetic.FULL}[name]
+    pc = synthetic.PRESETS[name]
     p = binding.Planner(pc, max_horizon=max_horizon, max_chunk=max_chunk)
     p.load_weights(weights_for(name))
     return p

@@ -36,7 +36,8 @@ def test_every_declared_symbol_is_exported(cdll):
 
 def test_blob_size_matches_packer(cdll):
     lib = binding.load(build_lib.LIB)
-    for pc, H in ((synthetic.TINY, 1), (synthetic.SMALL, 2)):
+    for pc, H in ((synthetic.TINY, 1), (synthetic.SMALL, 2), (synthetic.TINY_GATED, 1),
+                  (synthetic.SMALL_GATED, 2)):
         cfg = binding.make_config(pc, H)
         weights = synthetic.make_weights(pc)
         assert lib.jepa_weight_blob_bytes(ctypes.byref(cfg)) == len(binding.pack_weights(pc, weights))
@@ -50,6 +51,12 @@ def test_invalid_configs_rejected_without_gpu(cdll):
     bf = binding.make_config(synthetic.SMALL, 1)
     bf.heads = 12                       # bf16 path needs head dim 64
     assert lib.jepa_weight_blob_bytes(ctypes.byref(bf)) == 0
+    gq = binding.make_config(synthetic.SMALL_GATED, 1)
+    gq.mlp = 192                        # bf16 gated needs m % 128 == 0
+    assert lib.jepa_weight_blob_bytes(ctypes.byref(gq)) == 0
+    gq.mlp_kind = 2                     # unknown MLP kind
+    gq.mlp = 256
+    assert lib.jepa_weight_blob_bytes(ctypes.byref(gq)) == 0
     h = ctypes.c_void_p()
     assert lib.jepa_create(ctypes.byref(bad), 0, ctypes.byref(h)) == 2   # JEPA_ERR_SHAPE
     assert lib.jepa_status_string(6) == b"device wait timed out"

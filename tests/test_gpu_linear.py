@@ -58,3 +58,54 @@ def test_gelu_epilogue_against_exact_erf(planner):
     ref = predictor.gelu(A.astype(np.float64))
     err = np.abs(host(out) - ref)
     assert np.max(err / np.maximum(1.0, np.abs(ref))) < 2e-6, np.max(err)
+
+
+def _interleave32(a, b):
+    """Rows (or entries) of a and b in alternating blocks of 32: a[0:32], b[0:32], a[32:64], ..."""
+    n = a.shape[0]
+    out = np.empty((2 * n,) + a.shape[1:], a.dtype)
+    for p in range(n // 32):
+        out[64 * p:64 * p + 32] = a[32 * p:32 * p + 32]
+        out[64 * p + 32:64 * p + 64] = b[32 * p:32 * p + 32]
+    return out
+
+
+@pytest.mark.parametrize("M,n,K", [(300, 128, 192),      # ragged M, one tile of 4 pairs
+                                   (1000, 1536, 384),    # small predictor's up-projection
+                                   (129, 512, 1024),
+                                   (4100, 1536, 384)])   # > 1 tile per CTA, both accumulators
+def test_gated_linear_matches_definition(planner, M, n, K):
+    """Gated up-projection (FC1 * GELU(gate)) in one GEMM over interleaved weights, against
+    the definition computed with the two matrices separately."""
+    rng = np.random.default_rng(M + n + K)
+    A = predictor.round_to_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    W1 = predictor.round_to_bf16((rng.standard_normal((n, K)) * 0.05).astype(np.float32))
+    Wg = predictor.round_to_bf16((rng.standard_normal((n, K)) * 0.05).astype(np.float32))
+    b1 = rng.standard_normal(n).astype(np.float32)
+    bg = rng.standard_normal(n).astype(np.float32)
+    W = _interleave32(W1, Wg)
+    bias = _interleave32(b1, bg)
+    out = torch.zeros(M, n, device="cuda")
+    planner.linear_bf16(cuda(_bf16_bits(A).astype(np.int16)), cuda(_bf16_bits(W).astype(np.int16)),
+                        cuda(bias), M, 2 * n, K, 2, out)
+    planner.sync_check()
+    A64 = A.astype(np.float64)
+    ref = (A64 @ W1.astype(np.float64).T + b1) * predictor.gelu(A64 @ Wg.astype(np.float64).T + bg)
+    got = host(out)
+    scale = (np.sqrt(K) * 0.05 + 1.0) ** 2
+    assert np.max(np.abs(got - ref)) < 2e-5 * scale * 10, np.max(np.abs(got - ref))
+    # the wrong pairing (GELU on FC1) is far off: the test can tell the branches apart
+    swapped = predictor.gelu(A64 @ W1.astype(np.float64).T + b1) * (A64 @ Wg.astype(np.float64).T + bg)
+    assert np.max(np.abs(got - swapped)) > 1e-2
+
+
+def test_gated_linear_rejects_bad_shapes(planner):
+    from cem_search_transformer_gb300.binding import JepaError
+    A = torch.zeros(64, 64, dtype=torch.int16, device="cuda")
+    W = torch.zeros(384, 64, dtype=torch.int16, device="cuda")
+    out = torch.zeros(64, 192, device="cuda")
+    bias = torch.zeros(384, device="cuda")
+    with pytest.raises(JepaError):
+        planner.linear_bf16(A, W, bias, 64, 384, 64, 2, out)      # N not a multiple of 256
+    with pytest.raises(JepaError):
+        planner.linear_bf16(A, W[:256], None, 64, 256, 64, 2, out)  # gated needs a bias

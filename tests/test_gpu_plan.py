@@ -168,3 +168,16 @@ def test_plan_errors_and_kernel_count():
     # seed + context projection + R x (sample, pass, select/refit) + winner
     assert p.kernel_count(1, 1, 64, 8, R) == 1 + 1 + R * (1 + per_pass + 1) + 1
     p.close()
+
+
+def test_small_gated_plan_teacher_forced():
+    wl = synthetic.WORKLOADS["small_gated"]
+    pc = wl.predictor
+    p = make_planner("small_gated", max_horizon=wl.horizon)
+    z0, goal, s0 = synthetic.make_problems(pc, 1)
+    mu0, sg0 = synthetic.make_gaussian(pc, 1, wl.horizon)
+    out, tr = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    _teacher_forced("small_gated", pc, wl, z0, goal, s0, tr, 0, TOL_BF16_ENERGY_REL,
+                    sample=range(0, 200, 23))
+    assert np.array_equal(out[0], tr["actions"][-1, 0][tr["winner"][0], 0])
+    p.close()
