@@ -181,9 +181,8 @@ jepa_status jepa_cem_warm_start(jepa_ctx* ctx, const float* mu_prev, const float
                                 const float* sigma_prior, int B, int H, float* mu_out,
                                 float* sigma_out, void* stream);
 
-/* One step of the world model standing in for the robot (the closed-loop tests of the same
- * section use the world model as the simulator): the executed action goes through the
- * predictor with horizon 1.
+/* One step of the world model playing the robot, as in that section's closed-loop
+ * experiments: the executed action goes through the predictor with horizon 1.
  *   z [B,P,E], state [B,S], action [B,A]: dev inputs
  *   z_next [B,P,E] dev   output: the predicted next frame (must not overlap z)
  *   state_next [B,S] dev output: state + action (may equal state)

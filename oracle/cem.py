@@ -17,8 +17,8 @@ Readings taken where the page is silent:
 
 Receding-horizon control (same page, section "Further Optimization", parts A and B):
 the robot executes one action per planning step and the next step may be seeded from
-the previous plan instead of a fresh Gaussian; the closed-loop tests there use the
-world model itself as the simulator. Readings taken:
+the previous plan instead of a fresh Gaussian; that section's closed-loop experiments
+let the predictor play the robot. Readings taken:
   * warm start: the last round's mean loses its executed first step, the remaining
     H-1 steps move one step earlier, and the newly exposed last step takes the prior's
     mean; every step's width restarts at the prior's sigma (re-using the mean, not the
