@@ -39,20 +39,27 @@ __host__ __device__ constexpr int epi_warps(int mode) {
   return (mode == EPI_GELU || mode == EPI_GATED) ? 16 : 8;
 }
 __host__ __device__ constexpr int cta_threads(int mode) { return 64 + 32 * epi_warps(mode); }
+// Per-warp staging floats: the GELU epilogue transposes bf16 results (32 rows x 64 B), the
+// others fp32 accumulators (32 x 32 x 4 B).
+__host__ __device__ constexpr int stg_floats(int mode) { return mode == EPI_GELU ? 512 : STG_FLOATS; }
 
-template <int BN, int EW>
+template <int BN, int MODE>
 struct Cfg {
+  static constexpr int EW = epi_warps(MODE);
+  static constexpr int STG = stg_floats(MODE);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? (EW > 8 ? 3 : 4) : (EW > 8 ? 5 : 6);
+  // as many ring stages (up to 6) as the shared memory left by the staging buffers holds
+  static constexpr int FIT = (232448 - 1024 - 16 - 5 * 8 - EW * STG * 4) / (STAGE_BYTES + 16);
+  static constexpr int STAGES = FIT < 6 ? FIT : 6;
   static constexpr int TMEM_COLS = 2 * BN;   // two accumulators; 256 or 512 (power of 2)
   // ring, epilogue transpose buffers, barriers (full/empty per stage, tfull/tempty per
   // accumulator, teardown), TMEM address slot + abort flag, 1024 B alignment slack
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = STG_OFF + EW * STG_FLOATS * 4;
+  static constexpr int BAR_OFF = STG_OFF + EW * STG * 4;
   static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(STAGES >= 3 && SMEM <= 232448, "shared memory budget");
 };
 
 // 2-SM tiles: a CTA pair computes 256 x 256 (each CTA 128 rows, all 256 columns in its TMEM);
@@ -155,6 +162,114 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
   return true;
 }
 
+
+// GELU epilogue (EPI_GELU): each lane owns one accumulator row. Bias and GELU are applied in
+// that layout straight from TMEM (the bias is the same for every lane: broadcast loads), and
+// only the bf16 results go through the warp's staging buffer (32 rows x 64 B, 16-byte pieces
+// swizzled by row) so that the global stores are row-contiguous. Staging bf16 instead of
+// fp32 halves the buffer, which leaves room for one more stage of the operand ring. With
+// fp32 output (the C-ABI linear layer) rows are stored directly.
+template <int BN, int EW, typename Release>
+__device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, int N, int m0,
+                                                   int n_blk, uint32_t tmem_acc, uint32_t tfull,
+                                                   uint32_t tfull_parity, uint32_t tempty,
+                                                   Release release, float* stg_f, int ew, int warp,
+                                                   int lane, volatile int* abort_flag,
+                                                   int* err_flag) {
+  const int quarter = warp & 3;
+  const int part = ew >> 2;
+  constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp
+  const int cbase = n_blk * BN + part * SPAN;
+  int nvalid = 0;
+  while (nvalid < SPAN / 32 && cbase + 32 * nvalid < N) ++nvalid;
+  uint8_t* stg = reinterpret_cast<uint8_t*>(stg_f);
+  if (!mbar_wait(tfull, tfull_parity, abort_flag, err_flag)) return false;
+  tc_fence_after();
+  const uint32_t tbase = tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * SPAN);
+  const int row_base = m0 + quarter * 32;
+  uint32_t r[32];
+  if (nvalid > 0) tmem_ld32_async(tbase, r);
+#pragma unroll
+  for (int j = 0; j < SPAN / 32; ++j) {
+    if (j >= nvalid) break;
+    tmem_wait(r);
+    if (j == nvalid - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release(tempty);
+    }
+    const int c0 = cbase + 32 * j;
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = c0 + 4 * k;
+      const float4 b = (epi.bias && c < N) ? __ldg(reinterpret_cast<const float4*>(epi.bias + c))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 g = gelu4(make_float4(__uint_as_float(r[4 * k]) + b.x,
+                                         __uint_as_float(r[4 * k + 1]) + b.y,
+                                         __uint_as_float(r[4 * k + 2]) + b.z,
+                                         __uint_as_float(r[4 * k + 3]) + b.w));
+      v[4 * k] = g.x;
+      v[4 * k + 1] = g.y;
+      v[4 * k + 2] = g.z;
+      v[4 * k + 3] = g.w;
+    }
+    if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);   // r is free again
+    const int row = row_base + lane;
+    if (!epi.act_bf16) {
+      if (row < M) {
+        float* orow = reinterpret_cast<float*>(epi.out0) + map_row(epi.map0, row) * epi.ld0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (c0 + 4 * k < N)
+            *reinterpret_cast<float4*>(orow + c0 + 4 * k) =
+                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      }
+      continue;
+    }
+    // row `lane`, 16-byte piece q (8 columns) at byte lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)
+    const int swz = (lane >> 1) & 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u;
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q], v[8 * q + 1]);
+      __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+      __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+      u.x = *reinterpret_cast<uint32_t*>(&h0);
+      u.y = *reinterpret_cast<uint32_t*>(&h1);
+      u.z = *reinterpret_cast<uint32_t*>(&h2);
+      u.w = *reinterpret_cast<uint32_t*>(&h3);
+      *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ swz) << 4)) = u;
+    }
+    __syncwarp();
+    // 128 pieces of 16 bytes; lane takes pieces lane + 32 i: rows (lane >> 2) + 8 i, piece lane & 3
+    const int q = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int rr = (lane >> 2) + 8 * i;
+      const uint4 u = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((q ^ ((rr >> 1) & 3)) << 4));
+      const int grow = row_base + rr;
+      const int col = c0 + 8 * q;
+      if (grow < M && col < N) {
+        bf16* dst = reinterpret_cast<bf16*>(epi.out0) + map_row(epi.map0, grow) * epi.ld0 + col;
+        if (col + 8 <= N) {
+          *reinterpret_cast<uint4*>(dst) = u;
+        } else {                              // N % 8 == 4: the last 4 columns
+          *reinterpret_cast<uint2*>(dst) = make_uint2(u.x, u.y);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  if (nvalid == 0) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) release(tempty);
+  }
+  return true;
+}
+
 template <int BN, int MODE, int EW, typename Release>
 __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N, int m0, int n_blk,
                                               uint32_t tmem_acc, uint32_t tfull,
@@ -165,6 +280,9 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
     static_assert(BN == 256, "gated tiles hold four FC1/gate block pairs");
     return epilogue_tile_gated<EW>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity, tempty,
                                    release, stg, ew, warp, lane, abort_flag, err_flag);
+  } else if constexpr (MODE == EPI_GELU) {
+    return epilogue_tile_gelu<BN, EW>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity, tempty,
+                                      release, stg, ew, warp, lane, abort_flag, err_flag);
   } else {
   const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
   const int part = ew >> 2;                  // which share of the tile's columns
@@ -320,7 +438,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int M, int N, int K, Epilogue epi, int* err_flag) {
   constexpr int EW = epi_warps(MODE);
-  using C = Cfg<BN, EW>;
+  using C = Cfg<BN, MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -443,7 +561,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
   } else {
     // ---------------- epilogue (warps 2..) ----------------
     const int ew = warp - 2;
-    float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * STG_FLOATS;
+    float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * C::STG;
     int acc = 0;
     uint32_t acc_phase = 0;
     auto release = [](uint32_t bar) { mbar_arrive(bar); };
@@ -621,7 +739,7 @@ int gemm_tc_partials(int N) {
 template <int BN, int MODE>
 static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                              int* err_flag, int num_sms, cudaStream_t s) {
-  using C = Cfg<BN, epi_warps(MODE)>;
+  using C = Cfg<BN, MODE>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, MODE>,
