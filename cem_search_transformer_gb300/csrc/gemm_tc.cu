@@ -39,9 +39,11 @@ __host__ __device__ constexpr int epi_warps(int mode) {
   return (mode == EPI_GELU || mode == EPI_GATED) ? 16 : 8;
 }
 __host__ __device__ constexpr int cta_threads(int mode) { return 64 + 32 * epi_warps(mode); }
-// Per-warp staging floats: the GELU epilogue transposes bf16 results (32 rows x 64 B), the
-// others fp32 accumulators (32 x 32 x 4 B).
-__host__ __device__ constexpr int stg_floats(int mode) { return mode == EPI_GELU ? 512 : STG_FLOATS; }
+// Per-warp staging floats: the GELU and gated epilogues transpose bf16 results (32 rows x
+// 64 B), the others fp32 accumulators (32 x 32 x 4 B).
+__host__ __device__ constexpr int stg_floats(int mode) {
+  return (mode == EPI_GELU || mode == EPI_GATED) ? 512 : STG_FLOATS;
+}
 
 template <int BN, int MODE>
 struct Cfg {
@@ -84,17 +86,74 @@ struct Cfg2 {
 // accumulator through `release(tempty)` as soon as its last TMEM load has landed, then
 // finishes the global stores. Returns false if a bounded wait expired.
 
+// Stores 32 consecutive output columns [c0, c0 + 32) of rows row_base .. row_base + 31,
+// lane i holding row row_base + i in v[0..31]. bf16 output goes through the warp's staging
+// buffer (32 rows x 64 B, 16-byte pieces swizzled by row) so that the global stores are
+// row-contiguous; fp32 output (the C-ABI linear layer) is stored row by row.
+__device__ __forceinline__ bool store_rows32(const Epilogue& epi, int M, int N, int row_base,
+                                             int c0, const float (&v)[32], float* stg_f,
+                                             int lane) {
+  const int row = row_base + lane;
+  if (!epi.act_bf16) {
+    if (row < M) {
+      float* orow = reinterpret_cast<float*>(epi.out0) + map_row(epi.map0, row) * epi.ld0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (c0 + 4 * k < N)
+          *reinterpret_cast<float4*>(orow + c0 + 4 * k) =
+              make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+    }
+    return true;
+  }
+  uint8_t* stg = reinterpret_cast<uint8_t*>(stg_f);
+  // row `lane`, 16-byte piece q (8 columns) at byte lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)
+  const int swz = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q], v[8 * q + 1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+    u.x = *reinterpret_cast<uint32_t*>(&h0);
+    u.y = *reinterpret_cast<uint32_t*>(&h1);
+    u.z = *reinterpret_cast<uint32_t*>(&h2);
+    u.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ swz) << 4)) = u;
+  }
+  __syncwarp();
+  // 128 pieces of 16 bytes; lane takes pieces lane + 32 i: rows (lane >> 2) + 8 i, piece lane & 3
+  const int q = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rr = (lane >> 2) + 8 * i;
+    const uint4 u = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((q ^ ((rr >> 1) & 3)) << 4));
+    const int grow = row_base + rr;
+    const int col = c0 + 8 * q;
+    if (grow < M && col < N) {
+      bf16* dst = reinterpret_cast<bf16*>(epi.out0) + map_row(epi.map0, grow) * epi.ld0 + col;
+      if (col + 8 <= N) {
+        *reinterpret_cast<uint4*>(dst) = u;
+      } else {                                // N % 8 == 4: the last 4 columns
+        *reinterpret_cast<uint2*>(dst) = make_uint2(u.x, u.y);
+      }
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
 // Gated-MLP epilogue (EPI_GATED, 256-column tiles, 16 epilogue warps): each warp owns a
 // 32-row quarter and 64 accumulator columns, i.e. exactly one FC1 block and the gate block
 // that follows it in the interleaved weight. Per half of 16 columns the lane loads its row's
-// FC1 and gate values from TMEM, forms (fc1 + b) * gelu(gate + b) in place, and the 32 outputs
-// of the row go through the warp's staging buffer so that stores are row-contiguous.
+// FC1 and gate values from TMEM and forms (fc1 + b) * gelu(gate + b); the row's 32 outputs
+// then leave like the GELU epilogue's (bf16 staging, row-contiguous stores).
 template <int EW, typename Release>
 __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, int N, int m0,
                                                     int n_blk, uint32_t tmem_acc, uint32_t tfull,
                                                     uint32_t tfull_parity, uint32_t tempty,
-                                                    Release release, float* stg, int ew, int warp,
-                                                    int lane, volatile int* abort_flag,
+                                                    Release release, float* stg_f, int ew,
+                                                    int warp, int lane, volatile int* abort_flag,
                                                     int* err_flag) {
   static_assert(EW == 16, "one FC1/gate block pair per epilogue warp");
   const int quarter = warp & 3;
@@ -106,6 +165,7 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
   tc_fence_after();
   const uint32_t tbase = tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * 64);
   uint32_t r[32];
+  float v[32];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     if (active) {
@@ -124,44 +184,20 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
       const int c = cbase + 16 * half + 4 * k;
       const float4 b1 = __ldg(reinterpret_cast<const float4*>(epi.bias + c));
       const float4 bg = __ldg(reinterpret_cast<const float4*>(epi.bias + c + 32));
-      float4 g = make_float4(__uint_as_float(r[16 + 4 * k]) + bg.x,
-                             __uint_as_float(r[16 + 4 * k + 1]) + bg.y,
-                             __uint_as_float(r[16 + 4 * k + 2]) + bg.z,
-                             __uint_as_float(r[16 + 4 * k + 3]) + bg.w);
-      g = gelu4(g);
-      const float4 h = make_float4((__uint_as_float(r[4 * k]) + b1.x) * g.x,
-                                   (__uint_as_float(r[4 * k + 1]) + b1.y) * g.y,
-                                   (__uint_as_float(r[4 * k + 2]) + b1.z) * g.z,
-                                   (__uint_as_float(r[4 * k + 3]) + b1.w) * g.w);
-      const int q = 4 * half + k;            // float4 group of the row's 32 outputs
-      *reinterpret_cast<float4*>(stg + lane * 32 + ((q ^ (lane & 7)) << 2)) = h;
+      const float4 g = gelu4(make_float4(__uint_as_float(r[16 + 4 * k]) + bg.x,
+                                         __uint_as_float(r[16 + 4 * k + 1]) + bg.y,
+                                         __uint_as_float(r[16 + 4 * k + 2]) + bg.z,
+                                         __uint_as_float(r[16 + 4 * k + 3]) + bg.w));
+      float* o = v + 16 * half + 4 * k;
+      o[0] = (__uint_as_float(r[4 * k]) + b1.x) * g.x;
+      o[1] = (__uint_as_float(r[4 * k + 1]) + b1.y) * g.y;
+      o[2] = (__uint_as_float(r[4 * k + 2]) + b1.z) * g.z;
+      o[3] = (__uint_as_float(r[4 * k + 3]) + b1.w) * g.w;
     }
   }
   if (!active) return true;
-  __syncwarp();
-  const int cg = lane & 7, rsub = lane >> 3;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = rsub + 4 * i;
-    const int row = m0 + quarter * 32 + rr;
-    const float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
-    if (row >= M) continue;
-    const long long off = map_row(epi.map0, row) * epi.ld0 + ocol + 4 * cg;
-    if (epi.act_bf16) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo);
-      u.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(epi.out0) + off) = u;
-    } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(epi.out0) + off) = v;
-    }
-  }
-  __syncwarp();
-  return true;
+  return store_rows32(epi, M, N, m0 + quarter * 32, ocol, v, stg_f, lane);
 }
-
 
 // GELU epilogue (EPI_GELU): each lane owns one accumulator row. Bias and GELU are applied in
 // that layout straight from TMEM (the bias is the same for every lane: broadcast loads), and
@@ -182,7 +218,6 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
   const int cbase = n_blk * BN + part * SPAN;
   int nvalid = 0;
   while (nvalid < SPAN / 32 && cbase + 32 * nvalid < N) ++nvalid;
-  uint8_t* stg = reinterpret_cast<uint8_t*>(stg_f);
   if (!mbar_wait(tfull, tfull_parity, abort_flag, err_flag)) return false;
   tc_fence_after();
   const uint32_t tbase = tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * SPAN);
@@ -215,52 +250,7 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
       v[4 * k + 3] = g.w;
     }
     if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);   // r is free again
-    const int row = row_base + lane;
-    if (!epi.act_bf16) {
-      if (row < M) {
-        float* orow = reinterpret_cast<float*>(epi.out0) + map_row(epi.map0, row) * epi.ld0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (c0 + 4 * k < N)
-            *reinterpret_cast<float4*>(orow + c0 + 4 * k) =
-                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-      }
-      continue;
-    }
-    // row `lane`, 16-byte piece q (8 columns) at byte lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)
-    const int swz = (lane >> 1) & 3;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 u;
-      __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q], v[8 * q + 1]);
-      __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-      __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-      u.x = *reinterpret_cast<uint32_t*>(&h0);
-      u.y = *reinterpret_cast<uint32_t*>(&h1);
-      u.z = *reinterpret_cast<uint32_t*>(&h2);
-      u.w = *reinterpret_cast<uint32_t*>(&h3);
-      *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ swz) << 4)) = u;
-    }
-    __syncwarp();
-    // 128 pieces of 16 bytes; lane takes pieces lane + 32 i: rows (lane >> 2) + 8 i, piece lane & 3
-    const int q = lane & 3;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int rr = (lane >> 2) + 8 * i;
-      const uint4 u = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((q ^ ((rr >> 1) & 3)) << 4));
-      const int grow = row_base + rr;
-      const int col = c0 + 8 * q;
-      if (grow < M && col < N) {
-        bf16* dst = reinterpret_cast<bf16*>(epi.out0) + map_row(epi.map0, grow) * epi.ld0 + col;
-        if (col + 8 <= N) {
-          *reinterpret_cast<uint4*>(dst) = u;
-        } else {                              // N % 8 == 4: the last 4 columns
-          *reinterpret_cast<uint2*>(dst) = make_uint2(u.x, u.y);
-        }
-      }
-    }
-    __syncwarp();
+    store_rows32(epi, M, N, row_base, c0, v, stg_f, lane);
   }
   if (nvalid == 0) {
     tc_fence_before();
