@@ -17,7 +17,8 @@ module docstrings state the reading taken.
 Modules:
   philox     counter-based Philox4x32-10 + Box-Muller candidate sampler
   predictor  pre-LN block-causal transformer predictor, rollout, L1 energy
-  cem        elite selection, Gaussian refit, the round loop
+  cem        elite selection, Gaussian refit, the round loop, warm start, closed loop
+  quant      fp8 e4m3 quantisation of the LayerNorm-fed GEMMs (low-precision mode)
 
 Pins (tests/test_oracle_*.py): cuRAND's host Philox4_32_10 stream, hand-derived
 Box-Muller closed forms, torch.nn.TransformerEncoderLayer / layer_norm / gelu,
@@ -25,4 +26,4 @@ brute-force per-token attention loops, block-causality and permutation
 invariants, brute-force sort for top-K, closed-form refit moments, and CEM
 convergence to the closed-form optimum of a linear-quadratic problem.
 """
-from . import philox, predictor, cem  # noqa: F401
+from . import philox, quant, predictor, cem  # noqa: F401

@@ -30,6 +30,10 @@ definition; a KV cache reaches the same values because of block causality.
 In bf16 mode the matrices that the CUDA path stores in bf16 (W_in, W_qkv, W_o, W_1,
 W_g, W_2, W_out) are rounded to bf16 (round to nearest even) before upcasting; all
 activations stay float64.
+
+In fp8 mode (``quant.py``) the GEMMs fed by a LayerNorm (QKV, MLP up, projection to E) take
+per-channel scaled e4m3 weights and per-row scaled e4m3 copies of the LayerNorm output; the
+other matrices are bf16 as in bf16 mode.
 """
 from __future__ import annotations
 
@@ -38,7 +42,10 @@ from typing import Dict, List
 import numpy as np
 from scipy.special import erf
 
+from . import quant
+
 MATRIX_SUFFIXES = ("W_in", "W_qkv", "W_o", "W_1", "W_g", "W_2", "W_out")
+FP8_SUFFIXES = ("W_qkv", "W_1", "W_g", "W_out")      # fp8 mode: e4m3 with row scales
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
@@ -50,14 +57,26 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def prepare_weights(w: Dict[str, np.ndarray], precision: str) -> Dict[str, np.ndarray]:
-    """float64 copies of the fp32 weights; bf16 mode rounds the GEMM matrices first."""
+    """float64 copies of the fp32 weights; bf16 mode rounds the GEMM matrices first; fp8
+    mode quantises the LayerNorm-fed GEMM matrices per output channel instead."""
     out = {}
     for name, v in w.items():
         v = np.asarray(v, np.float32)
-        if precision == "bf16" and name.split(".")[-1] in MATRIX_SUFFIXES:
+        kind = name.split(".")[-1]
+        if precision == "fp8" and kind in FP8_SUFFIXES:
+            out[name] = quant.fake_quant_rows(v.astype(np.float64))
+            continue
+        if precision in ("bf16", "fp8") and kind in MATRIX_SUFFIXES:
             v = round_to_bf16(v)
         out[name] = v.astype(np.float64)
+    if precision == "fp8":
+        out["__fp8__"] = np.ones(1)               # marks the activation quantisation
     return out
+
+
+def _gemm_input(w: Dict[str, np.ndarray], h: np.ndarray) -> np.ndarray:
+    """What a LayerNorm-fed GEMM multiplies: h itself, or in fp8 mode its per-row e4m3 copy."""
+    return quant.fake_quant_rows(h) if "__fp8__" in w else h
 
 
 def layer_norm(x: np.ndarray, g: np.ndarray, b: np.ndarray, eps: float) -> np.ndarray:
@@ -94,13 +113,13 @@ def transformer_layer(x: np.ndarray, w: Dict[str, np.ndarray], l: int, heads: in
     """One pre-LN layer on x [n, L, d]."""
     n, L, d = x.shape
     hd = d // heads
-    h = layer_norm(x, w[f"l{l}.ln1_g"], w[f"l{l}.ln1_b"], eps)
+    h = _gemm_input(w, layer_norm(x, w[f"l{l}.ln1_g"], w[f"l{l}.ln1_b"], eps))
     qkv = h @ w[f"l{l}.W_qkv"].T + w[f"l{l}.b_qkv"]                  # [n, L, 3d]
     q, k, v = (qkv[..., i * d:(i + 1) * d].reshape(n, L, heads, hd).transpose(0, 2, 1, 3)
                for i in range(3))
     o = attention(q, k, v, allowed).transpose(0, 2, 1, 3).reshape(n, L, d)
     x = x + o @ w[f"l{l}.W_o"].T + w[f"l{l}.b_o"]
-    h2 = layer_norm(x, w[f"l{l}.ln2_g"], w[f"l{l}.ln2_b"], eps)
+    h2 = _gemm_input(w, layer_norm(x, w[f"l{l}.ln2_g"], w[f"l{l}.ln2_b"], eps))
     fc1 = h2 @ w[f"l{l}.W_1"].T + w[f"l{l}.b_1"]
     if f"l{l}.W_g" in w:                                  # gated MLP
         u = fc1 * gelu(h2 @ w[f"l{l}.W_g"].T + w[f"l{l}.b_g"])
@@ -140,7 +159,8 @@ def rollout(w: Dict[str, np.ndarray], cfg, z0: np.ndarray, state0: np.ndarray,
         for l in range(cfg.layers):
             x = transformer_layer(x, w, l, cfg.heads, allowed, cfg.ln_eps)
         xp = x[:, k * T + 2:(k + 1) * T]                              # patches of block k
-        z_next = layer_norm(xp, w["lnf_g"], w["lnf_b"], cfg.ln_eps) @ w["W_out"].T + w["b_out"]
+        z_next = _gemm_input(w, layer_norm(xp, w["lnf_g"], w["lnf_b"], cfg.ln_eps)) @ w["W_out"].T \
+            + w["b_out"]
         preds.append(z_next)
         frames.append(z_next)
     return preds
