@@ -18,7 +18,10 @@ a format. Readings taken:
     per-row scale exists without another pass), as do the in-projection of z and the
     action / state embeddings;
   * the product of two codes is exact in fp32 and the GEMM accumulates in fp32; the result
-    is multiplied by s_row * s_col before the bias.
+    is multiplied by s_row * s_col before the bias;
+  * a code is an integer decided by floating point, so it is decided in the CUDA path's
+    precision: the row maximum, the factor 448 / max and the scaled value are fp32
+    (each operation rounded), then rounded to e4m3; the scale is max / 448 in fp32.
 """
 from __future__ import annotations
 
@@ -42,11 +45,15 @@ def round_to_e4m3(x: np.ndarray) -> np.ndarray:
 
 
 def quantize_rows(a: np.ndarray):
-    """Per-row scaled e4m3: returns (codes as float64 values, scales [rows])."""
-    a = np.asarray(a, np.float64)
-    amax = np.max(np.abs(a), axis=-1)
-    s = np.where(amax > 0, amax / E4M3_MAX, 1.0)
-    return round_to_e4m3(a / s[..., None]), s
+    """Per-row scaled e4m3: returns (codes as float64 values, scales [rows] as float64)."""
+    a32 = np.asarray(a, np.float64).astype(np.float32)
+    amax = np.max(np.abs(a32), axis=-1)
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1))
+    inv = np.where(nz, np.float32(E4M3_MAX) / safe, np.float32(1)).astype(np.float32)
+    v = (a32 * inv[..., None]).astype(np.float32)
+    s = np.where(nz, safe / np.float32(E4M3_MAX), np.float32(1)).astype(np.float32)
+    return round_to_e4m3(v), s.astype(np.float64)
 
 
 def fake_quant_rows(a: np.ndarray) -> np.ndarray:

@@ -55,16 +55,17 @@ def test_row_scaling_closed_forms():
     rng = np.random.default_rng(1)
     a = rng.standard_normal((5, 37))
     q, s = quant.quantize_rows(a)
-    assert np.allclose(s, np.max(np.abs(a), axis=1) / 448.0, rtol=0, atol=0)
+    assert np.allclose(s, np.max(np.abs(a), axis=1) / 448.0, rtol=1e-7, atol=0)
     assert np.array_equal(np.max(np.abs(q), axis=1), np.full(5, 448.0))   # the row max -> 448
     assert np.array_equal(quant.round_to_e4m3(q), q)                     # codes are e4m3
     # power-of-two scaling moves only the scale
     q2, s2 = quant.quantize_rows(a * 8.0)
     assert np.array_equal(q2, q) and np.array_equal(s2, s * 8.0)
-    # a zero row keeps scale 1 and zero codes; a constant row is exact
+    # a zero row keeps scale 1 and zero codes; a constant row with exact scale is exact
     qz, sz = quant.quantize_rows(np.zeros((1, 4)))
     assert np.array_equal(qz, np.zeros((1, 4))) and sz[0] == 1.0
-    assert np.array_equal(quant.fake_quant_rows(np.full((1, 6), -0.3)), np.full((1, 6), -0.3))
+    c = -448.0 * 2.0 ** -10          # scale 2^-10 and factor 1024 are exact in fp32
+    assert np.array_equal(quant.fake_quant_rows(np.full((1, 6), c)), np.full((1, 6), c))
     # the relative error of any non-tiny element is at most half an e4m3 step (2^-4)
     fq = quant.fake_quant_rows(a)
     big = np.abs(a) >= np.max(np.abs(a), axis=1, keepdims=True) / 448.0 * 2.0 ** -6
