@@ -27,7 +27,7 @@ EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string
            "jepa_plan_kernel_count", "jepa_linear_bf16", "jepa_profile_enable",
            "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc",
            "jepa_attention_bf16", "jepa_cem_warm_start", "jepa_world_model_step",
-           "jepa_cem_closed_loop")
+           "jepa_cem_closed_loop", "jepa_linear_fp8", "jepa_quantize_rows_fp8")
 
 
 class JepaError(RuntimeError):
@@ -45,6 +45,7 @@ class Config(ctypes.Structure):
                 ("max_chunk", ctypes.c_int32), ("mlp_kind", ctypes.c_int32)]
 
 MLP_KINDS = {"gelu": 0, "gated": 1}
+PRECISIONS = {"fp32": 0, "bf16": 1, "fp8": 2}
 
 
 class Trace(ctypes.Structure):
@@ -85,6 +86,8 @@ def load(path: str = _LIB_PATH):
         "jepa_cem_warm_start": ([P, P, P, P, I, I, P, P, P], I),
         "jepa_world_model_step": ([P, P, P, P, I, P, P, P, P, P], I),
         "jepa_cem_closed_loop": ([P, P, P, P, P, P, I, I, I, I, I, I, I, U64, P, P, P], I),
+        "jepa_linear_fp8": ([P, P, P, P, P, P, I, I, I, I, P, P], I),
+        "jepa_quantize_rows_fp8": ([P, P, I, I, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -96,7 +99,7 @@ def load(path: str = _LIB_PATH):
 
 def make_config(pc: synthetic.PredictorConfig, max_horizon: int = 1, max_chunk: int = 0) -> Config:
     return Config(pc.layers, pc.width, pc.heads, pc.mlp, pc.patch_tokens, pc.embed_dim,
-                  pc.action_dim, pc.state_dim, max_horizon, 1 if pc.precision == "bf16" else 0,
+                  pc.action_dim, pc.state_dim, max_horizon, PRECISIONS[pc.precision],
                   pc.ln_eps, max_chunk, MLP_KINDS[pc.mlp_kind])
 
 
@@ -243,6 +246,16 @@ class Planner:
     def linear_bf16(self, A, W, bias, M, N, K, gelu, out, stream=None):
         self._check(self.lib.jepa_linear_bf16(self.h, _ptr(A), _ptr(W), _ptr(bias), M, N, K,
                                               int(gelu), _ptr(out), _stream(stream)), "linear_bf16")
+
+    def linear_fp8(self, A, a_scale, W, w_scale, bias, M, N, K, gelu, out, stream=None):
+        self._check(self.lib.jepa_linear_fp8(self.h, _ptr(A), _ptr(a_scale), _ptr(W), _ptr(w_scale),
+                                             _ptr(bias), M, N, K, int(gelu), _ptr(out),
+                                             _stream(stream)), "linear_fp8")
+
+    def quantize_rows_fp8(self, x, rows, cols, codes, scales, stream=None):
+        self._check(self.lib.jepa_quantize_rows_fp8(self.h, _ptr(x), rows, cols, _ptr(codes),
+                                                    _ptr(scales), _stream(stream)),
+                    "quantize_rows_fp8")
 
     def attention_bf16(self, q, kv, out, ncand, T, Lk, kv_rows, heads, d, stream=None):
         self._check(self.lib.jepa_attention_bf16(self.h, _ptr(q), _ptr(kv), _ptr(out), ncand, T, Lk,

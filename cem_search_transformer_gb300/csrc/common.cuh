@@ -57,6 +57,10 @@ struct Epilogue {
   int cands_per_problem; // N of the plan (candidate -> problem)
   float* partial;        // [M, ntiles] per-tile (and per column half) sums of |z - goal|
   int ntiles;            // partial sums per row (energy finalisation adds all of them)
+  // fp8 operands only: accumulator (r, c) is multiplied by row_scale[r] * col_scale[c]
+  // (activation row scale, weight output-channel scale) before the bias
+  const float* row_scale;
+  const float* col_scale;
 };
 
 // GELU with the Gaussian CDF written through erf: x * (1 + erf(x / sqrt 2)) / 2.
@@ -232,6 +236,9 @@ __device__ __forceinline__ float epi_apply4(const Epilogue& e, const EpiRow& w, 
 // tcgen05 / TMA GEMM: out = epilogue(A[M,K] * W[N,K]^T), bf16 in, fp32 accumulate.
 cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                          int* err_flag, int num_sms, cudaStream_t s);
+// fp8 e4m3 operands (codes), scales in epi.row_scale / epi.col_scale; K a multiple of 16
+cudaError_t gemm_tc_fp8(const uint8_t* A, const uint8_t* W, int M, int N, int K,
+                        const Epilogue& epi, int* err_flag, int num_sms, cudaStream_t s);
 // Energy partial sums per row that the tensor-core GEMM writes for an output width N.
 int gemm_tc_partials(int N);
 
@@ -250,8 +257,12 @@ cudaError_t attention_f32(const float* q, const float* kv, float* o, int ncand, 
                           long long kv_cand_stride_rows, int heads, int d, cudaStream_t s);
 
 // LayerNorm of fp32 rows (gathered through in_map) into bf16 or fp32 rows.
-cudaError_t layernorm(const float* x, RowMap in_map, void* y, int y_bf16, const float* g,
-                      const float* b, int rows, int d, float eps, cudaStream_t s);
+// out_kind: 0 fp32, 1 bf16, 2 fp8 e4m3 codes (row scales to yscale)
+cudaError_t layernorm(const float* x, RowMap in_map, void* y, int out_kind, const float* g,
+                      const float* b, int rows, int d, float eps, cudaStream_t s,
+                      float* yscale = nullptr);
+cudaError_t quantize_rows_fp8(const float* src, long long rows, int cols, uint8_t* codes,
+                              float* scales, cudaStream_t s);
 
 // Philox4x32-10 + Box-Muller candidate sampler (seed from *seed_dev if non-null).
 cudaError_t sample_actions(const float* mu, const float* sigma, int B, int N, int H, int A,

@@ -148,7 +148,7 @@ __device__ __forceinline__ bool store_rows32(const Epilogue& epi, int M, int N, 
 // that follows it in the interleaved weight. Per half of 16 columns the lane loads its row's
 // FC1 and gate values from TMEM and forms (fc1 + b) * gelu(gate + b); the row's 32 outputs
 // then leave like the GELU epilogue's (bf16 staging, row-contiguous stores).
-template <int EW, typename Release>
+template <int EW, int OP, typename Release>
 __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, int N, int m0,
                                                     int n_blk, uint32_t tmem_acc, uint32_t tfull,
                                                     uint32_t tfull_parity, uint32_t tempty,
@@ -164,6 +164,8 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
   if (!mbar_wait(tfull, tfull_parity, abort_flag, err_flag)) return false;
   tc_fence_after();
   const uint32_t tbase = tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * 64);
+  float rs = 1.f;                            // fp8: this lane's row scale
+  if constexpr (OP) rs = (m0 + quarter * 32 + lane < M) ? epi.row_scale[m0 + quarter * 32 + lane] : 0.f;
   uint32_t r[32];
   float v[32];
 #pragma unroll
@@ -184,15 +186,22 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
       const int c = cbase + 16 * half + 4 * k;
       const float4 b1 = __ldg(reinterpret_cast<const float4*>(epi.bias + c));
       const float4 bg = __ldg(reinterpret_cast<const float4*>(epi.bias + c + 32));
-      const float4 g = gelu4(make_float4(__uint_as_float(r[16 + 4 * k]) + bg.x,
-                                         __uint_as_float(r[16 + 4 * k + 1]) + bg.y,
-                                         __uint_as_float(r[16 + 4 * k + 2]) + bg.z,
-                                         __uint_as_float(r[16 + 4 * k + 3]) + bg.w));
+      float4 f = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                             __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+      float4 q = make_float4(__uint_as_float(r[16 + 4 * k]), __uint_as_float(r[16 + 4 * k + 1]),
+                             __uint_as_float(r[16 + 4 * k + 2]), __uint_as_float(r[16 + 4 * k + 3]));
+      if constexpr (OP) {
+        const float4 c1 = __ldg(reinterpret_cast<const float4*>(epi.col_scale + c));
+        const float4 cg = __ldg(reinterpret_cast<const float4*>(epi.col_scale + c + 32));
+        f.x *= rs * c1.x; f.y *= rs * c1.y; f.z *= rs * c1.z; f.w *= rs * c1.w;
+        q.x *= rs * cg.x; q.y *= rs * cg.y; q.z *= rs * cg.z; q.w *= rs * cg.w;
+      }
+      const float4 g = gelu4(make_float4(q.x + bg.x, q.y + bg.y, q.z + bg.z, q.w + bg.w));
       float* o = v + 16 * half + 4 * k;
-      o[0] = (__uint_as_float(r[4 * k]) + b1.x) * g.x;
-      o[1] = (__uint_as_float(r[4 * k + 1]) + b1.y) * g.y;
-      o[2] = (__uint_as_float(r[4 * k + 2]) + b1.z) * g.z;
-      o[3] = (__uint_as_float(r[4 * k + 3]) + b1.w) * g.w;
+      o[0] = (f.x + b1.x) * g.x;
+      o[1] = (f.y + b1.y) * g.y;
+      o[2] = (f.z + b1.z) * g.z;
+      o[3] = (f.w + b1.w) * g.w;
     }
   }
   if (!active) return true;
@@ -205,7 +214,7 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
 // swizzled by row) so that the global stores are row-contiguous. Staging bf16 instead of
 // fp32 halves the buffer, which leaves room for one more stage of the operand ring. With
 // fp32 output (the C-ABI linear layer) rows are stored directly.
-template <int BN, int EW, typename Release>
+template <int BN, int EW, int OP, typename Release>
 __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, int N, int m0,
                                                    int n_blk, uint32_t tmem_acc, uint32_t tfull,
                                                    uint32_t tfull_parity, uint32_t tempty,
@@ -222,6 +231,8 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
   tc_fence_after();
   const uint32_t tbase = tmem_acc + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * SPAN);
   const int row_base = m0 + quarter * 32;
+  float rs = 1.f;                            // fp8: this lane's row scale
+  if constexpr (OP) rs = (row_base + lane < M) ? epi.row_scale[row_base + lane] : 0.f;
   uint32_t r[32];
   if (nvalid > 0) tmem_ld32_async(tbase, r);
 #pragma unroll
@@ -240,10 +251,14 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
       const int c = c0 + 4 * k;
       const float4 b = (epi.bias && c < N) ? __ldg(reinterpret_cast<const float4*>(epi.bias + c))
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 g = gelu4(make_float4(__uint_as_float(r[4 * k]) + b.x,
-                                         __uint_as_float(r[4 * k + 1]) + b.y,
-                                         __uint_as_float(r[4 * k + 2]) + b.z,
-                                         __uint_as_float(r[4 * k + 3]) + b.w));
+      float4 a = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                             __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+      if constexpr (OP) {
+        const float4 cs = c < N ? __ldg(reinterpret_cast<const float4*>(epi.col_scale + c))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        a.x *= rs * cs.x; a.y *= rs * cs.y; a.z *= rs * cs.z; a.w *= rs * cs.w;
+      }
+      const float4 g = gelu4(make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
       v[4 * k] = g.x;
       v[4 * k + 1] = g.y;
       v[4 * k + 2] = g.z;
@@ -260,7 +275,7 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
   return true;
 }
 
-template <int BN, int MODE, int EW, typename Release>
+template <int BN, int MODE, int EW, int OP, typename Release>
 __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N, int m0, int n_blk,
                                               uint32_t tmem_acc, uint32_t tfull,
                                               uint32_t tfull_parity, uint32_t tempty,
@@ -268,11 +283,11 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
                                               int lane, volatile int* abort_flag, int* err_flag) {
   if constexpr (MODE == EPI_GATED) {
     static_assert(BN == 256, "gated tiles hold four FC1/gate block pairs");
-    return epilogue_tile_gated<EW>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity, tempty,
-                                   release, stg, ew, warp, lane, abort_flag, err_flag);
+    return epilogue_tile_gated<EW, OP>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
+                                       tempty, release, stg, ew, warp, lane, abort_flag, err_flag);
   } else if constexpr (MODE == EPI_GELU) {
-    return epilogue_tile_gelu<BN, EW>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity, tempty,
-                                      release, stg, ew, warp, lane, abort_flag, err_flag);
+    return epilogue_tile_gelu<BN, EW, OP>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
+                                          tempty, release, stg, ew, warp, lane, abort_flag, err_flag);
   } else {
   const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
   const int part = ew >> 2;                  // which share of the tile's columns
@@ -309,12 +324,20 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
   float esum[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) esum[i] = 0.f;
+  // fp8 operands: per-row (activation) and per-column (weight) scales of the accumulators
+  float rsc[8];
+  if constexpr (OP) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rsc[i] = ((vmask >> i) & 1) ? epi.row_scale[row0 + 4 * i] : 0.f;
+  }
   int nvalid = 0;
   while (nvalid < SPAN / 32 && cbase + 32 * nvalid < N) ++nvalid;
-  float4 nxt[8], nbias = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 nxt[8], nbias = make_float4(0.f, 0.f, 0.f, 0.f), ncs = make_float4(0.f, 0.f, 0.f, 0.f);
   auto fetch = [&](int c) {
     const bool ok = c < N;
     nbias = ok ? epi_bias4(epi, c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (OP)
+      ncs = ok ? __ldg(reinterpret_cast<const float4*>(epi.col_scale + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
     if constexpr (kResid) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -360,6 +383,7 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
     const bool col_ok = c < N;
     float4 cur[8];
     const float4 bb = nbias;
+    const float4 cs = ncs;
     if constexpr (!kStore) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
@@ -373,6 +397,9 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
       const int rr = rsub + 4 * i;
       float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
       if (!(((vmask >> i) & 1) && col_ok)) continue;
+      if constexpr (OP) {
+        v.x *= rsc[i] * cs.x; v.y *= rsc[i] * cs.y; v.z *= rsc[i] * cs.z; v.w *= rsc[i] * cs.w;
+      }
       v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
       if constexpr (kStore) {
         if (MODE == EPI_GELU) v = gelu4(v);
@@ -423,7 +450,10 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
   }
 }
 
-template <int BN, int MODE>
+// OP 0: bf16 operands (kind::f16, 64 elements of K per 128-byte row); OP 1: fp8 e4m3
+// operands (kind::f8f6f4, 128 elements per row) with per-row / per-column scales applied in
+// the epilogue. Stages hold the same bytes either way.
+template <int BN, int MODE, int OP>
 __global__ void __launch_bounds__(cta_threads(MODE), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int M, int N, int K, Epilogue epi, int* err_flag) {
@@ -445,7 +475,8 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
   const int num_n = (N + BN - 1) / BN;
   const int num_m = (M + BM - 1) / BM;
   const int total = num_m * num_n;
-  const int num_k = (K + BK - 1) / BK;
+  constexpr int BKE = OP ? 2 * BK : BK;        // K elements per stage (128 bytes per row)
+  const int num_k = (K + BKE - 1) / BKE;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -490,8 +521,8 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
           }
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
-          tma_load_2d(sa, &tmA, kb * BK, m0, full_bar(stage));
-          tma_load_2d(sa + C::A_BYTES, &tmB, kb * BK, n0, full_bar(stage));
+          tma_load_2d(sa, &tmA, kb * BKE, m0, full_bar(stage));
+          tma_load_2d(sa + C::A_BYTES, &tmB, kb * BKE, n0, full_bar(stage));
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == C::STAGES) stage = 0, phase ^= 1u;
@@ -511,7 +542,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      constexpr uint32_t idesc = OP ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -532,8 +563,12 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
           const uint64_t bdesc = desc_sw128(sa + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // advance 16 bf16 = 32 bytes along K inside the swizzle atom (+2 in 16-byte units)
-            mma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+            // advance 32 bytes along K inside the swizzle atom (+2 in 16-byte units): 16 bf16
+            // or 32 e4m3 elements per MMA
+            if constexpr (OP)
+              mma_e4m3_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+            else
+              mma_bf16_ss(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
           }
           mma_commit(empty_bar(stage));
           if (++stage == C::STAGES) stage = 0, phase ^= 1u;
@@ -557,7 +592,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
     auto release = [](uint32_t bar) { mbar_arrive(bar); };
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const int m0 = (t / num_n) * BM, n_blk = t % num_n;
-      if (!epilogue_tile<BN, MODE, EW>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
+      if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
                                        tfull_bar(acc), acc_phase, tempty_bar(acc), release, stg, ew,
                                        warp, lane, abort_flag, err_flag))
         break;
@@ -578,7 +613,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
 // to the "smem empty" and "accumulator full" barriers of both CTAs; each CTA's epilogue drains
 // its own 128 rows and releases the accumulator on the leader's barrier. Halving the operand
 // bytes each SM stages per MMA keeps shared-memory traffic within its bandwidth.
-template <int MODE>
+template <int MODE, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                int M, int N, int K, Epilogue epi, int* err_flag) {
@@ -603,7 +638,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
   const int num_n = (N + BN - 1) / BN;
   const int num_m = (M + 2 * BM - 1) / (2 * BM);
   const int total = num_m * num_n;
-  const int num_k = (K + BK - 1) / BK;
+  constexpr int BKE = OP ? 2 * BK : BK;        // K elements per stage (128 bytes per row)
+  const int num_k = (K + BKE - 1) / BKE;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -642,8 +678,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t lfull = map_to_rank(full_bar(stage), 0);
           if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
-          tma_load_2d_pair(sa, &tmA, kb * BK, m0, lfull);
-          tma_load_2d_pair(sa + C::A_BYTES, &tmB, kb * BK, n0, lfull);
+          tma_load_2d_pair(sa, &tmA, kb * BKE, m0, lfull);
+          tma_load_2d_pair(sa + C::A_BYTES, &tmB, kb * BKE, n0, lfull);
           issued_any = true;
           if (++stage == C::STAGES) stage = 0, phase ^= 1u;
         }
@@ -659,7 +695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (leader only) ----------------
-      constexpr uint32_t idesc = idesc_bf16(2 * BM, BN);
+      constexpr uint32_t idesc = OP ? idesc_e4m3(2 * BM, BN) : idesc_bf16(2 * BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -679,8 +715,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
           const uint64_t adesc = desc_sw128(sa);
           const uint64_t bdesc = desc_sw128(sa + C::A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            if constexpr (OP)
+              mma_e4m3_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+            else
+              mma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          }
           mma_commit_pair_both(empty_bar(stage));
           if (++stage == C::STAGES) stage = 0, phase ^= 1u;
         }
@@ -702,7 +742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
     auto release = [](uint32_t bar) { mbar_arrive_cluster(bar); };
     for (int t = cid; t < total; t += ncl) {
       const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n_blk = t % num_n;
-      if (!epilogue_tile<BN, MODE, EW>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
+      if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
                                        tfull_bar(acc), acc_phase, map_to_rank(tempty_bar(acc), 0),
                                        release, stg, ew, warp, lane, abort_flag, err_flag))
         break;
@@ -726,90 +766,104 @@ int gemm_tc_partials(int N) {
   return (epi_warps(EPI_OUTPROJ) / 4) * ((N + tile_n(N) - 1) / tile_n(N));
 }
 
-template <int BN, int MODE>
-static cudaError_t launch_tc(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
+template <int OP>
+static bool operand_map(CUtensorMap* m, const void* p, int rows, int cols, int box_rows) {
+  return OP ? make_map_u8(m, p, rows, cols, box_rows) : make_map(m, p, rows, cols, box_rows);
+}
+
+template <int BN, int MODE, int OP>
+static cudaError_t launch_tc(const void* A, const void* W, int M, int N, int K, const Epilogue& epi,
                              int* err_flag, int num_sms, cudaStream_t s) {
   using C = Cfg<BN, MODE>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, MODE>,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, MODE, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, W, N, K, BN)) return cudaErrorInvalidValue;
+  if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, BN))
+    return cudaErrorInvalidValue;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  k_gemm_tc<BN, MODE><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  k_gemm_tc<BN, MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
   return cudaGetLastError();
 }
 
-template <int BN>
-static cudaError_t launch_mode(const bf16* A, const bf16* W, int M, int N, int K,
+template <int BN, int OP>
+static cudaError_t launch_mode(const void* A, const void* W, int M, int N, int K,
                                const Epilogue& epi, int* err_flag, int num_sms, cudaStream_t s) {
   switch (epi.mode) {
-    case EPI_STORE: return launch_tc<BN, EPI_STORE>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_GELU: return launch_tc<BN, EPI_GELU>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_RESID: return launch_tc<BN, EPI_RESID>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_INPROJ: return launch_tc<BN, EPI_INPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_OUTPROJ: return launch_tc<BN, EPI_OUTPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_STORE: return launch_tc<BN, EPI_STORE, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_GELU: return launch_tc<BN, EPI_GELU, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_OUTPROJ: return launch_tc<BN, EPI_OUTPROJ, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    case EPI_GATED:
+      if constexpr (BN == 256) return launch_tc<256, EPI_GATED, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
+      return cudaErrorInvalidValue;
+    default: break;
+  }
+  if constexpr (OP == 0) {   // the residual and in-projection GEMMs have bf16 operands only
+    switch (epi.mode) {
+      case EPI_RESID: return launch_tc<BN, EPI_RESID, 0>(A, W, M, N, K, epi, err_flag, num_sms, s);
+      case EPI_INPROJ: return launch_tc<BN, EPI_INPROJ, 0>(A, W, M, N, K, epi, err_flag, num_sms, s);
+      default: break;
+    }
   }
   return cudaErrorInvalidValue;
 }
 
-template <>
-cudaError_t launch_mode<256>(const bf16* A, const bf16* W, int M, int N, int K,
-                             const Epilogue& epi, int* err_flag, int num_sms, cudaStream_t s) {
-  switch (epi.mode) {
-    case EPI_STORE: return launch_tc<256, EPI_STORE>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_GELU: return launch_tc<256, EPI_GELU>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_RESID: return launch_tc<256, EPI_RESID>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_INPROJ: return launch_tc<256, EPI_INPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_OUTPROJ: return launch_tc<256, EPI_OUTPROJ>(A, W, M, N, K, epi, err_flag, num_sms, s);
-    case EPI_GATED: return launch_tc<256, EPI_GATED>(A, W, M, N, K, epi, err_flag, num_sms, s);
-  }
-  return cudaErrorInvalidValue;
-}
-
-template <int MODE>
-static cudaError_t launch_tc2(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
+template <int MODE, int OP>
+static cudaError_t launch_tc2(const void* A, const void* W, int M, int N, int K, const Epilogue& epi,
                               int* err_flag, int num_sms, cudaStream_t s) {
   using C = Cfg2<epi_warps(MODE)>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2<MODE, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, W, N, K, 128)) return cudaErrorInvalidValue;
+  if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, 128))
+    return cudaErrorInvalidValue;
   const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
   const int pairs = num_sms / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  k_gemm_tc2<MODE><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  k_gemm_tc2<MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
   return cudaGetLastError();
+}
+
+template <int OP>
+static cudaError_t gemm_tc(const void* A, const void* W, int M, int N, int K, const Epilogue& epi,
+                           int* err_flag, int num_sms, cudaStream_t s) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  // TMA: 16-byte aligned bases and row strides
+  if (K <= 0 || K % (OP ? 16 : 8) != 0 || N % 4 != 0 || (((uintptr_t)A) & 15) ||
+      (((uintptr_t)W) & 15))
+    return cudaErrorInvalidValue;
+  if (epi.mode == EPI_STORE && (epi.split % 32) != 0) return cudaErrorInvalidValue;
+  if (epi.mode == EPI_GATED && (N % 256 != 0 || !epi.bias)) return cudaErrorInvalidValue;
+  if (OP && (!epi.row_scale || !epi.col_scale)) return cudaErrorInvalidValue;
+  // QKV and the residual projections (N a multiple of 256, many row tiles) run on CTA
+  // pairs; the GELU layer keeps single CTAs, whose 16 epilogue warps need the registers
+  if (N % 256 == 0 && M >= 4 * BM && num_sms >= 2) {
+    if (epi.mode == EPI_STORE) return launch_tc2<EPI_STORE, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    if constexpr (OP == 0)
+      if (epi.mode == EPI_RESID) return launch_tc2<EPI_RESID, 0>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  }
+  if (tile_n(N) == 256) return launch_mode<256, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  return launch_mode<128, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
 }
 
 cudaError_t gemm_tc_bf16(const bf16* A, const bf16* W, int M, int N, int K, const Epilogue& epi,
                          int* err_flag, int num_sms, cudaStream_t s) {
-  if (M <= 0 || N <= 0) return cudaSuccess;
-  if (K <= 0 || K % 8 != 0 || N % 4 != 0 || (((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
-    return cudaErrorInvalidValue;
-  if (epi.mode == EPI_STORE && (epi.split % 32) != 0) return cudaErrorInvalidValue;
-  if (epi.mode == EPI_GATED && (N % 256 != 0 || !epi.bias)) return cudaErrorInvalidValue;
-  // QKV and the residual projections (N a multiple of 256, many row tiles) run on CTA
-  // pairs; the GELU layer keeps single CTAs, whose 16 epilogue warps need the registers
-  if (N % 256 == 0 && M >= 4 * BM && num_sms >= 2) {
-    switch (epi.mode) {
-      case EPI_STORE: return launch_tc2<EPI_STORE>(A, W, M, N, K, epi, err_flag, num_sms, s);
-      case EPI_RESID: return launch_tc2<EPI_RESID>(A, W, M, N, K, epi, err_flag, num_sms, s);
-      default: break;
-    }
-  }
-  if (tile_n(N) == 256) return launch_mode<256>(A, W, M, N, K, epi, err_flag, num_sms, s);
-  return launch_mode<128>(A, W, M, N, K, epi, err_flag, num_sms, s);
+  return gemm_tc<0>(A, W, M, N, K, epi, err_flag, num_sms, s);
+}
+
+cudaError_t gemm_tc_fp8(const uint8_t* A, const uint8_t* W, int M, int N, int K,
+                        const Epilogue& epi, int* err_flag, int num_sms, cudaStream_t s) {
+  return gemm_tc<1>(A, W, M, N, K, epi, err_flag, num_sms, s);
 }
 
 }  // namespace jepa

@@ -149,10 +149,20 @@ cudaError_t assemble_block(const float* actions, const float* state0, const floa
 // ---------------------------------------------------------------------------------
 // LayerNorm: one warp per row, fp32 statistics (two passes over registers).
 // ---------------------------------------------------------------------------------
-template <int VPL, bool OUT_BF16>
+// e4m3 code of x (round to nearest even, saturating to +-448): the low byte of a converted
+// pair whose two inputs are both x.
+__device__ __forceinline__ uint8_t e4m3_code(float x) {
+  uint16_t p;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(p) : "f"(x));
+  return (uint8_t)(p & 0xFF);
+}
+
+// Output kinds of the LayerNorm: 0 fp32, 1 bf16, 2 fp8 e4m3 codes with one scale per row
+// (scale = max |row| / 448, codes = e4m3(row * (448 / max |row|)); a zero row has scale 1).
+template <int VPL, int OUT>
 __global__ void k_layernorm(const float* __restrict__ x, RowMap in_map, void* __restrict__ y,
-                            const float* __restrict__ g, const float* __restrict__ bta, int rows,
-                            int d, float eps) {
+                            float* __restrict__ yscale, const float* __restrict__ g,
+                            const float* __restrict__ bta, int rows, int d, float eps) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows) return;
@@ -178,38 +188,92 @@ __global__ void k_layernorm(const float* __restrict__ x, RowMap in_map, void* __
 #pragma unroll
   for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
   const float rstd = rsqrtf(q / d + eps);
+  if constexpr (OUT == 2) {
+    float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int c = lane + 32 * i;
-    if (c < d) {
-      const float t = (v[i] - mean) * rstd * g[c] + bta[c];
-      if (OUT_BF16)
-        reinterpret_cast<bf16*>(y)[(long long)warp * d + c] = __float2bfloat16_rn(t);
-      else
-        reinterpret_cast<float*>(y)[(long long)warp * d + c] = t;
+    for (int i = 0; i < VPL; ++i) {
+      const int c = lane + 32 * i;
+      if (c < d) {
+        v[i] = (v[i] - mean) * rstd * g[c] + bta[c];
+        amax = fmaxf(amax, fabsf(v[i]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float inv = amax > 0.f ? 448.f / amax : 1.f;
+    if (lane == 0) yscale[warp] = amax > 0.f ? amax / 448.f : 1.f;
+    uint8_t* yr = reinterpret_cast<uint8_t*>(y) + (long long)warp * d;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int c = lane + 32 * i;
+      if (c < d) yr[c] = e4m3_code(v[i] * inv);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int c = lane + 32 * i;
+      if (c < d) {
+        const float t = (v[i] - mean) * rstd * g[c] + bta[c];
+        if (OUT == 1)
+          reinterpret_cast<bf16*>(y)[(long long)warp * d + c] = __float2bfloat16_rn(t);
+        else
+          reinterpret_cast<float*>(y)[(long long)warp * d + c] = t;
+      }
     }
   }
 }
 
-template <int VPL>
-static cudaError_t launch_ln(const float* x, RowMap m, void* y, int y_bf16, const float* g,
-                             const float* b, int rows, int d, float eps, cudaStream_t s) {
+// Per-row fp8 quantisation of fp32 rows (weights at load time, and the C ABI): one warp per
+// row, the same scale rule and rounding as the LayerNorm's fp8 output.
+__global__ void k_quantize_rows(const float* __restrict__ src, long long rows, int cols,
+                                uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const float* xr = src + r * cols;
+  float amax = 0.f;
+  for (int c = lane; c < cols; c += 32) amax = fmaxf(amax, fabsf(xr[c]));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float inv = amax > 0.f ? 448.f / amax : 1.f;
+  if (lane == 0) scales[r] = amax > 0.f ? amax / 448.f : 1.f;
+  uint8_t* cr = codes + r * cols;
+  for (int c = lane; c < cols; c += 32) cr[c] = e4m3_code(xr[c] * inv);
+}
+
+cudaError_t quantize_rows_fp8(const float* src, long long rows, int cols, uint8_t* codes,
+                              float* scales, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
   const int threads = 256;
-  const unsigned blocks = (unsigned)(((long long)rows * 32 + threads - 1) / threads);
-  if (y_bf16)
-    k_layernorm<VPL, true><<<blocks, threads, 0, s>>>(x, m, y, g, b, rows, d, eps);
-  else
-    k_layernorm<VPL, false><<<blocks, threads, 0, s>>>(x, m, y, g, b, rows, d, eps);
+  const unsigned blocks = (unsigned)((rows * 32 + threads - 1) / threads);
+  k_quantize_rows<<<blocks, threads, 0, s>>>(src, rows, cols, codes, scales);
   return cudaGetLastError();
 }
 
-cudaError_t layernorm(const float* x, RowMap in_map, void* y, int y_bf16, const float* g,
-                      const float* b, int rows, int d, float eps, cudaStream_t s) {
+template <int VPL>
+static cudaError_t launch_ln(const float* x, RowMap m, void* y, float* yscale, int out_kind,
+                             const float* g, const float* b, int rows, int d, float eps,
+                             cudaStream_t s) {
+  const int threads = 256;
+  const unsigned blocks = (unsigned)(((long long)rows * 32 + threads - 1) / threads);
+  if (out_kind == 2)
+    k_layernorm<VPL, 2><<<blocks, threads, 0, s>>>(x, m, y, yscale, g, b, rows, d, eps);
+  else if (out_kind == 1)
+    k_layernorm<VPL, 1><<<blocks, threads, 0, s>>>(x, m, y, yscale, g, b, rows, d, eps);
+  else
+    k_layernorm<VPL, 0><<<blocks, threads, 0, s>>>(x, m, y, yscale, g, b, rows, d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t layernorm(const float* x, RowMap in_map, void* y, int out_kind, const float* g,
+                      const float* b, int rows, int d, float eps, cudaStream_t s,
+                      float* yscale) {
   if (rows <= 0) return cudaSuccess;
-  if (d <= 128) return launch_ln<4>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
-  if (d <= 512) return launch_ln<16>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
-  if (d <= 1024) return launch_ln<32>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
-  if (d <= 2048) return launch_ln<64>(x, in_map, y, y_bf16, g, b, rows, d, eps, s);
+  if (out_kind == 2 && !yscale) return cudaErrorInvalidValue;
+  if (d <= 128) return launch_ln<4>(x, in_map, y, yscale, out_kind, g, b, rows, d, eps, s);
+  if (d <= 512) return launch_ln<16>(x, in_map, y, yscale, out_kind, g, b, rows, d, eps, s);
+  if (d <= 1024) return launch_ln<32>(x, in_map, y, yscale, out_kind, g, b, rows, d, eps, s);
+  if (d <= 2048) return launch_ln<64>(x, in_map, y, yscale, out_kind, g, b, rows, d, eps, s);
   return cudaErrorInvalidValue;
 }
 

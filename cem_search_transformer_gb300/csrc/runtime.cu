@@ -31,11 +31,17 @@ struct LayerW {
   const float *ln1_g, *ln1_b, *b_qkv, *b_o, *ln2_g, *ln2_b, *b_1, *b_2;
   const void *W_qkv, *W_o, *W_1, *W_2;  // bf16 (bf16 mode) or fp32
   // gated MLP: W_1 and b_1 above point at the interleaved [FC1 | gate] pair (2m rows)
+  const uint8_t *W_qkv8 = nullptr, *W_18 = nullptr;   // fp8 mode: e4m3 codes
+  const float *s_qkv = nullptr, *s_1 = nullptr;        // and their channel scales
 };
 
 struct Weights {
   float* f32 = nullptr;   // device copy of every tensor (blob minus header)
   bf16* mats = nullptr;   // bf16 copies of the GEMM matrices (bf16 mode)
+  uint8_t* q8 = nullptr;  // fp8 mode: e4m3 codes of W_qkv, W_1 (or the gated pair), W_out
+  float* q8s = nullptr;   // fp8 mode: their per-output-channel scales
+  const uint8_t* W_out8 = nullptr;
+  const float* s_out = nullptr;
   void* gmat = nullptr;   // gated MLP: per layer W_1 / W_g rows interleaved in blocks of 32
   float* gbias = nullptr; // gated MLP: per layer b_1 / b_g interleaved the same way
   const float *b_in, *W_a, *b_a, *W_s, *b_s, *pos, *lnf_g, *lnf_b, *b_out;
@@ -74,6 +80,7 @@ struct jepa_ctx {
   float* x = nullptr;
   void *xn = nullptr, *q = nullptr, *kv = nullptr, *o = nullptr, *hbuf = nullptr, *zhat = nullptr;
   float* partial = nullptr;
+  float* xs = nullptr;   // fp8 mode: row scales of the LayerNorm output in xn
   int ntiles = 0;
   // scratch for jepa_predictor_forward (base + converted context)
   float* fw_base = nullptr;
@@ -112,7 +119,10 @@ jepa_status fail(jepa_ctx* c, jepa_status s, const char* fmt, ...) {
                   "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
   } while (0)
 
-inline bool bf16_mode(const jepa_ctx* c) { return c->cfg.precision == JEPA_BF16; }
+// bf16 activations and tensor-core path (the fp8 mode is the bf16 path with its
+// LayerNorm-fed GEMMs on e4m3 operands)
+inline bool bf16_mode(const jepa_ctx* c) { return c->cfg.precision != JEPA_FP32; }
+inline bool fp8_mode(const jepa_ctx* c) { return c->cfg.precision == JEPA_FP8; }
 inline int tokens(const jepa_ctx* c) { return c->cfg.patch_tokens + 2; }
 inline size_t act_bytes(const jepa_ctx* c) { return bf16_mode(c) ? 2 : 4; }
 
@@ -136,7 +146,7 @@ jepa_status validate_config(const jepa_config* c) {
       (c->mlp_kind != JEPA_MLP_GELU && c->mlp_kind != JEPA_MLP_GATED))
     return JEPA_ERR_SHAPE;
   const int hd = c->width / c->heads;
-  if (c->precision == JEPA_BF16) {
+  if (c->precision == JEPA_BF16 || c->precision == JEPA_FP8) {
     if (hd != 64 || c->width % 64 || c->embed_dim % 64 || c->mlp % 64) return JEPA_ERR_SHAPE;
     if (c->mlp_kind == JEPA_MLP_GATED && c->mlp % 128) return JEPA_ERR_SHAPE;
   } else if (c->precision == JEPA_FP32) {
@@ -203,7 +213,8 @@ jepa_status ensure_workspace(jepa_ctx* ctx, int chunk, int H) {
       (s = dalloc(ctx, ctx->ws_allocs, &ctx->o, rows * d * ab)) ||
       (s = dalloc(ctx, ctx->ws_allocs, &ctx->hbuf, rows * m * ab)) ||
       (s = dalloc(ctx, ctx->ws_allocs, &ctx->zhat, (size_t)chunk * P * E * ab)) ||
-      (s = dalloc(ctx, ctx->ws_allocs, &ctx->partial, (size_t)chunk * P * ctx->ntiles * 4))) {
+      (s = dalloc(ctx, ctx->ws_allocs, &ctx->partial, (size_t)chunk * P * ctx->ntiles * 4)) ||
+      (s = dalloc(ctx, ctx->ws_allocs, &ctx->xs, fp8_mode(ctx) ? rows * 4 : 256))) {
     free_list(ctx->ws_allocs);
     return s;
   }
@@ -238,7 +249,7 @@ Epilogue epi_base(const jepa_ctx* c, int mode) {
 // out = epilogue(A * W^T) on the path of the context's precision; optionally bracketed by
 // profiling events (graph capture).
 jepa_status gemm(jepa_ctx* ctx, const void* A, const void* W, int M, int N, int K,
-                 const Epilogue& e, cudaStream_t s, PlanGraph* prof) {
+                 const Epilogue& e, cudaStream_t s, PlanGraph* prof, bool fp8 = false) {
   if (M <= 0) return JEPA_OK;
   if (prof) {
     cudaEvent_t a, b;
@@ -249,7 +260,9 @@ jepa_status gemm(jepa_ctx* ctx, const void* A, const void* W, int M, int N, int 
     prof->ev_flops.push_back(2.0 * M * N * (double)K);
     CK(cudaEventRecordWithFlags(a, s, cudaEventRecordExternal));
   }
-  if (bf16_mode(ctx)) {
+  if (fp8) {
+    CK(gemm_tc_fp8((const uint8_t*)A, (const uint8_t*)W, M, N, K, e, ctx->dev_err, ctx->num_sms, s));
+  } else if (bf16_mode(ctx)) {
     CK(gemm_tc_bf16((const bf16*)A, (const bf16*)W, M, N, K, e, ctx->dev_err, ctx->num_sms, s));
   } else {
     CK(gemm_simt_f32((const float*)A, (const float*)W, M, N, K, e, s));
@@ -292,6 +305,9 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
   const long long kv_stride = (long long)ctx->ws_H * T;              // rows per candidate
   const size_t ab = act_bytes(ctx);
   const size_t kv_slot_elems = (size_t)chunk * kv_stride * 2 * d;
+  // LayerNorm output: fp32, bf16, or (fp8 mode) e4m3 codes with row scales in xs
+  const bool f8 = fp8_mode(ctx);
+  const int ln_out = f8 ? 2 : bf16_mode(ctx) ? 1 : 0;
   jepa_status st;
   for (long long c0 = 0; c0 < total; c0 += chunk) {
     const int nc = (int)((total - c0) < chunk ? (total - c0) : chunk);
@@ -313,8 +329,8 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
       for (int l = 0; l < L; ++l) {
         const LayerW& lw = ctx->w.layers[l];
         uint8_t* kv_slot = (uint8_t*)ctx->kv + (H > 1 ? (size_t)l * kv_slot_elems * ab : 0);
-        CK(layernorm(ctx->x, identity_map(), ctx->xn, bf16_mode(ctx), lw.ln1_g, lw.ln1_b, rows, d,
-                     c.ln_eps, s));
+        CK(layernorm(ctx->x, identity_map(), ctx->xn, ln_out, lw.ln1_g, lw.ln1_b, rows, d,
+                     c.ln_eps, s, ctx->xs));
         {
           Epilogue e = epi_base(ctx, EPI_STORE);
           e.bias = lw.b_qkv;
@@ -324,7 +340,13 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
           e.out1 = kv_slot;
           e.ld1 = 2 * d;
           e.map1 = RowMap{T, kv_stride, (long long)k * T};
-          if ((st = gemm(ctx, ctx->xn, lw.W_qkv, rows, 3 * d, d, e, s, prof))) return st;
+          if (f8) {
+            e.row_scale = ctx->xs;
+            e.col_scale = lw.s_qkv;
+          }
+          if ((st = gemm(ctx, ctx->xn, f8 ? (const void*)lw.W_qkv8 : lw.W_qkv, rows, 3 * d, d, e, s,
+                         prof, f8)))
+            return st;
         }
         if (bf16_mode(ctx)) {
           CK(attention_tc_bf16((const bf16*)ctx->q, (const bf16*)kv_slot, (bf16*)ctx->o, nc, T,
@@ -340,15 +362,21 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
           e.ld0 = d;
           if ((st = gemm(ctx, ctx->o, lw.W_o, rows, d, d, e, s, prof))) return st;
         }
-        CK(layernorm(ctx->x, identity_map(), ctx->xn, bf16_mode(ctx), lw.ln2_g, lw.ln2_b, rows, d,
-                     c.ln_eps, s));
+        CK(layernorm(ctx->x, identity_map(), ctx->xn, ln_out, lw.ln2_g, lw.ln2_b, rows, d,
+                     c.ln_eps, s, ctx->xs));
         {
           const bool gated = c.mlp_kind == JEPA_MLP_GATED;
           Epilogue e = epi_base(ctx, gated ? EPI_GATED : EPI_GELU);
           e.bias = lw.b_1;
           e.out0 = ctx->hbuf;
           e.ld0 = m;
-          if ((st = gemm(ctx, ctx->xn, lw.W_1, rows, gated ? 2 * m : m, d, e, s, prof))) return st;
+          if (f8) {
+            e.row_scale = ctx->xs;
+            e.col_scale = lw.s_1;
+          }
+          if ((st = gemm(ctx, ctx->xn, f8 ? (const void*)lw.W_18 : lw.W_1, rows, gated ? 2 * m : m, d,
+                         e, s, prof, f8)))
+            return st;
         }
         {
           Epilogue e = epi_base(ctx, EPI_RESID);
@@ -359,8 +387,8 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
         }
       }
       // final LayerNorm on the patch rows of this block, then the out-projection to E
-      CK(layernorm(ctx->x, RowMap{P, (long long)T, 2}, ctx->xn, bf16_mode(ctx), ctx->w.lnf_g,
-                   ctx->w.lnf_b, nc * P, d, c.ln_eps, s));
+      CK(layernorm(ctx->x, RowMap{P, (long long)T, 2}, ctx->xn, ln_out, ctx->w.lnf_g,
+                   ctx->w.lnf_b, nc * P, d, c.ln_eps, s, ctx->xs));
       {
         const bool last = (k == H - 1);
         Epilogue e = epi_base(ctx, EPI_OUTPROJ);
@@ -373,7 +401,13 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
         e.cands_per_problem = N;
         e.partial = ctx->partial;
         e.ntiles = ctx->ntiles;
-        if ((st = gemm(ctx, ctx->xn, ctx->w.W_out, nc * P, E, d, e, s, prof))) return st;
+        if (f8) {
+          e.row_scale = ctx->xs;
+          e.col_scale = ctx->w.s_out;
+        }
+        if ((st = gemm(ctx, ctx->xn, f8 ? (const void*)ctx->w.W_out8 : ctx->w.W_out, nc * P, E, d, e,
+                       s, prof, f8)))
+          return st;
       }
     }
     if (goal && energy)
@@ -543,6 +577,8 @@ void jepa_destroy(jepa_ctx* ctx) {
   if (ctx->w.mats) cudaFree(ctx->w.mats);
   if (ctx->w.gmat) cudaFree(ctx->w.gmat);
   if (ctx->w.gbias) cudaFree(ctx->w.gbias);
+  if (ctx->w.q8) cudaFree(ctx->w.q8);
+  if (ctx->w.q8s) cudaFree(ctx->w.q8s);
   if (ctx->fw_base) cudaFree(ctx->fw_base);
   if (ctx->fw_z) cudaFree(ctx->fw_z);
   if (ctx->dev_err) cudaFree(ctx->dev_err);
@@ -673,6 +709,37 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
       w.layers[l].W_2 = lm[4 * l + 3];
     }
   }
+  // fp8 mode: e4m3 codes with per-output-channel scales for the LayerNorm-fed GEMMs, per
+  // layer [W_qkv | W_1 (or the interleaved gated pair)], then W_out
+  const size_t mrows = gated ? 2 * m : m;
+  const size_t q8_layer = (3 * d + mrows) * d, q8s_layer = 3 * d + mrows;
+  if (fp8_mode(ctx)) {
+    e = cudaMalloc(&w.q8, c.layers * q8_layer + E * d);
+    if (e == cudaSuccess) e = cudaMalloc(&w.q8s, (c.layers * q8s_layer + E) * 4);
+    for (int l = 0; l < c.layers && e == cudaSuccess; ++l) {
+      uint8_t* q = w.q8 + l * q8_layer;
+      float* qs = w.q8s + l * q8s_layer;
+      e = quantize_rows_fp8(lm[4 * l], 3 * d, (int)d, q, qs, 0);
+      if (e == cudaSuccess && !gated) e = quantize_rows_fp8(lm[4 * l + 2], m, (int)d, q + 3 * d * d, qs + 3 * d, 0);
+      w.layers[l].W_qkv8 = q;
+      w.layers[l].s_qkv = qs;
+      w.layers[l].W_18 = q + 3 * d * d;
+      w.layers[l].s_1 = qs + 3 * d;
+    }
+    if (e == cudaSuccess)
+      e = quantize_rows_fp8(W_out, E, (int)d, w.q8 + c.layers * q8_layer, w.q8s + c.layers * q8s_layer, 0);
+    w.W_out8 = w.q8 + c.layers * q8_layer;
+    w.s_out = w.q8s + c.layers * q8s_layer;
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(f32);
+      if (w.mats) cudaFree(w.mats);
+      if (w.q8) cudaFree(w.q8);
+      if (w.q8s) cudaFree(w.q8s);
+      return fail(ctx, JEPA_ERR_CUDA, "fp8 weights: %s", cudaGetErrorString(e));
+    }
+  }
   if (gated) {
     // one up-projection GEMM per layer over [FC1 | gate] rows interleaved in blocks of 32
     // (2-D copies on the device), converted to bf16 in bf16 mode
@@ -696,6 +763,9 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
                          cudaMemcpyDeviceToDevice);
       if (e == cudaSuccess && bf16_mode(ctx))
         e = convert_f32_bf16(tmp, (bf16*)w.gmat + l * nmat, (long long)nmat, 0);
+      if (e == cudaSuccess && fp8_mode(ctx))
+        e = quantize_rows_fp8(tmp, 2 * m, (int)d, w.q8 + l * q8_layer + 3 * d * d,
+                              w.q8s + l * q8s_layer + 3 * d, 0);
       if (e == cudaSuccess && bf16_mode(ctx)) e = cudaDeviceSynchronize();  // tmp is reused
       if (e == cudaSuccess) {
         w.layers[l].W_1 = bf16_mode(ctx) ? (const void*)((bf16*)w.gmat + l * nmat)
@@ -710,6 +780,8 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
       if (w.mats) cudaFree(w.mats);
       if (w.gmat) cudaFree(w.gmat);
       if (w.gbias) cudaFree(w.gbias);
+      if (w.q8) cudaFree(w.q8);
+      if (w.q8s) cudaFree(w.q8s);
       return fail(ctx, JEPA_ERR_CUDA, "gated MLP weights: %s", cudaGetErrorString(e));
     }
   }
@@ -718,6 +790,8 @@ jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes
   if (ctx->w.mats) cudaFree(ctx->w.mats);
   if (ctx->w.gmat) cudaFree(ctx->w.gmat);
   if (ctx->w.gbias) cudaFree(ctx->w.gbias);
+  if (ctx->w.q8) cudaFree(ctx->w.q8);
+  if (ctx->w.q8s) cudaFree(ctx->w.q8s);
   ctx->w = w;
   ctx->loaded = true;
   return JEPA_OK;
@@ -975,6 +1049,39 @@ jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W
   e.ld0 = gelu == 2 ? N / 2 : N;
   CK(gemm_tc_bf16((const bf16*)A, (const bf16*)W, M, N, K, e, ctx->dev_err, ctx->num_sms,
                   (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
+jepa_status jepa_linear_fp8(jepa_ctx* ctx, const uint8_t* A, const float* a_scale,
+                            const uint8_t* W, const float* w_scale, const float* bias, int M,
+                            int N, int K, int gelu, float* out, void* stream) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  if (!bf16_mode(ctx)) return fail(ctx, JEPA_ERR_UNSUPPORTED, "linear_fp8 needs a bf16 or fp8 context");
+  if (bad_ptr(A) || bad_ptr(a_scale) || bad_ptr(W) || bad_ptr(w_scale) || bad_ptr(out) || M < 1 ||
+      N < 1 || K < 16 || K % 16 || N % 4 || gelu < 0 || gelu > 2 ||
+      (gelu == 2 && (N % 256 != 0 || !bias)))
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_fp8: bad argument");
+  if ((((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_fp8: A and W must be 16-byte aligned");
+  CK(cudaSetDevice(ctx->device));
+  Epilogue e = epi_base(ctx, gelu == 2 ? EPI_GATED : gelu ? EPI_GELU : EPI_STORE);
+  e.act_bf16 = 0;
+  e.bias = bias;
+  e.out0 = out;
+  e.ld0 = gelu == 2 ? N / 2 : N;
+  e.row_scale = a_scale;
+  e.col_scale = w_scale;
+  CK(gemm_tc_fp8(A, W, M, N, K, e, ctx->dev_err, ctx->num_sms, (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
+jepa_status jepa_quantize_rows_fp8(jepa_ctx* ctx, const float* x, int rows, int cols,
+                                   uint8_t* codes, float* scales, void* stream) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  if (bad_ptr(x) || bad_ptr(codes) || bad_ptr(scales) || rows < 1 || cols < 1)
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "quantize_rows_fp8: bad argument");
+  CK(cudaSetDevice(ctx->device));
+  CK(quantize_rows_fp8(x, rows, cols, codes, scales, (cudaStream_t)stream));
   return JEPA_OK;
 }
 

@@ -39,7 +39,7 @@ class PredictorConfig:
     embed_dim: int      # E
     action_dim: int = 7  # A
     state_dim: int = 7   # S
-    precision: str = "bf16"  # "fp32" or "bf16"
+    precision: str = "bf16"  # "fp32", "bf16" or "fp8" (bf16 with fp8 LayerNorm-fed GEMMs)
     ln_eps: float = 1e-5
     mlp_kind: str = "gelu"   # "gelu": W_2 GELU(W_1 x); "gated": W_2 (W_1 x * GELU(W_g x))
 
@@ -79,8 +79,14 @@ TINY_GATED = dataclasses.replace(TINY, name="tiny_gated", mlp_kind="gated")
 SMALL_GATED = dataclasses.replace(SMALL, name="small_gated", mlp_kind="gated")
 FULL_GATED = dataclasses.replace(FULL, name="full_gated", mlp_kind="gated")
 
+# Low-precision variants: the same predictors with their LayerNorm-fed GEMMs in fp8 e4m3.
+SMALL_FP8 = dataclasses.replace(SMALL, name="small_fp8", precision="fp8")
+FULL_FP8 = dataclasses.replace(FULL, name="full_fp8", precision="fp8")
+SMALL_GATED_FP8 = dataclasses.replace(SMALL_GATED, name="small_gated_fp8", precision="fp8")
+
 PRESETS: Dict[str, PredictorConfig] = {c.name: c for c in (TINY, SMALL, FULL, TINY_GATED,
-                                                            SMALL_GATED, FULL_GATED)}
+                                                            SMALL_GATED, FULL_GATED, SMALL_FP8,
+                                                            FULL_FP8, SMALL_GATED_FP8)}
 
 WORKLOADS: Dict[str, CemConfig] = {
     "tiny": CemConfig(TINY, B=1, N=64, K=8, rounds=2, horizon=1),
@@ -90,6 +96,8 @@ WORKLOADS: Dict[str, CemConfig] = {
     "tiny_gated": CemConfig(TINY_GATED, B=1, N=64, K=8, rounds=2, horizon=1),
     "small_gated": CemConfig(SMALL_GATED, B=1, N=200, K=20, rounds=5, horizon=2),
     "full_gated": CemConfig(FULL_GATED, B=1, N=800, K=80, rounds=10, horizon=1),
+    "small_fp8": CemConfig(SMALL_FP8, B=1, N=200, K=20, rounds=5, horizon=2),
+    "full_fp8": CemConfig(FULL_FP8, B=1, N=800, K=80, rounds=10, horizon=1),
 }
 for _n in (100, 200, 400, 800, 1600, 3200):
     for _b in (1, 4, 8):

@@ -50,7 +50,12 @@ typedef enum {
   JEPA_ERR_UNSUPPORTED = 7   /* device is not sm_103 / feature not built */
 } jepa_status;
 
-typedef enum { JEPA_FP32 = 0, JEPA_BF16 = 1 } jepa_precision;
+/* FP8: the bf16 path with the GEMMs fed by a LayerNorm (QKV, MLP up, projection to E) on
+ * fp8 e4m3 operands (kind::f8f6f4): weights with one scale per output channel, the
+ * LayerNorm output with one scale per row; everything else as in BF16. (The planning
+ * page's "Further Optimization", D, and the Realtime-VLA notes, 9.1, name 8-bit
+ * quantisation of the predictor as the way to shrink its compute.) */
+typedef enum { JEPA_FP32 = 0, JEPA_BF16 = 1, JEPA_FP8 = 2 } jepa_precision;
 
 /* MLP of each layer. GELU: u = GELU(W_1 h + b_1). GATED (the Realtime-VLA notes, section 4.2
  * "Fusing Gated Linear Layers": FC1(x, w1) * GELU(FC2(x, w2))): u = (W_1 h + b_1) *
@@ -70,7 +75,8 @@ typedef struct {
   int32_t action_dim;    /* A (7 in the planning workloads) */
   int32_t state_dim;     /* S (7) */
   int32_t max_horizon;   /* largest H any call will use; sizes the KV cache */
-  int32_t precision;     /* jepa_precision: FP32 = SIMT fp32 path, BF16 = tensor-core path */
+  int32_t precision;     /* jepa_precision: FP32 = SIMT fp32 path, BF16 = tensor-core path,
+                            FP8 = tensor-core path with fp8 LayerNorm-fed GEMMs */
   float ln_eps;          /* LayerNorm epsilon (1e-5) */
   int32_t max_chunk;     /* candidates per predictor pass (0 = library default); bounds workspace */
   int32_t mlp_kind;      /* jepa_mlp_kind */
@@ -223,6 +229,23 @@ jepa_status jepa_plan_kernel_count(jepa_ctx* ctx, int B, int H, int N, int K, in
 jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W,
                              const float* bias, int M, int N, int K, int gelu, float* out,
                              void* stream);
+
+/* The fp8 GEMM of the FP8 mode on caller data: out[M,N] = act((A[M,K] * W[N,K]^T) *
+ * a_scale[M] (rows) * w_scale[N] (columns) + bias[N]), A and W e4m3 codes (one byte each,
+ * OCP E4M3: bias 7, no infinities, largest 448), fp32 accumulation, fp32 output.
+ *   gelu: 0 identity, 1 erf GELU, 2 gated (as jepa_linear_bf16; out [M, N/2]).
+ *   K a multiple of 16; A, W 16-byte aligned dev; scales and bias dev. Needs a BF16 or FP8
+ *   context. */
+jepa_status jepa_linear_fp8(jepa_ctx* ctx, const uint8_t* A, const float* a_scale,
+                            const uint8_t* W, const float* w_scale, const float* bias, int M,
+                            int N, int K, int gelu, float* out, void* stream);
+
+/* Row-wise fp8 quantisation, the rule of the FP8 mode: per row r, scales[r] = max|x[r,:]| /
+ * 448 (1 for an all-zero row) and codes[r,c] = e4m3(x[r,c] * (448 / max|x[r,:]|)), rounded to
+ * nearest even and saturated (fp32 arithmetic: the division and the product each rounded).
+ *   x [rows, cols] float32 dev; codes [rows, cols] uint8 dev; scales [rows] float32 dev. */
+jepa_status jepa_quantize_rows_fp8(jepa_ctx* ctx, const float* x, int rows, int cols,
+                                   uint8_t* codes, float* scales, void* stream);
 
 /* Block-causal attention of one rollout step as the predictor runs it (bf16 mode): for each
  * candidate c and head h, queries q[c*T + t, h*64 : h*64+64] attend to cached key / value
