@@ -324,12 +324,8 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
   float esum[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) esum[i] = 0.f;
-  // fp8 operands: per-row (activation) and per-column (weight) scales of the accumulators
-  float rsc[8];
-  if constexpr (OP) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) rsc[i] = ((vmask >> i) & 1) ? epi.row_scale[row0 + 4 * i] : 0.f;
-  }
+  // fp8 operands: per-row (activation) and per-column (weight) scales of the accumulators;
+  // the row scales are read where they are used (L1-resident), not held in registers
   int nvalid = 0;
   while (nvalid < SPAN / 32 && cbase + 32 * nvalid < N) ++nvalid;
   float4 nxt[8], nbias = make_float4(0.f, 0.f, 0.f, 0.f), ncs = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -398,7 +394,8 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
       float4 v = *reinterpret_cast<const float4*>(stg + rr * 32 + ((cg ^ (rr & 7)) << 2));
       if (!(((vmask >> i) & 1) && col_ok)) continue;
       if constexpr (OP) {
-        v.x *= rsc[i] * cs.x; v.y *= rsc[i] * cs.y; v.z *= rsc[i] * cs.z; v.w *= rsc[i] * cs.w;
+        const float rsi = __ldg(epi.row_scale + row0 + 4 * i);
+        v.x *= rsi * cs.x; v.y *= rsi * cs.y; v.z *= rsi * cs.z; v.w *= rsi * cs.w;
       }
       v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
       if constexpr (kStore) {
