@@ -217,15 +217,14 @@ def run_ours(args, wl):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         return float(tt.item())
 
-    planner.profile_enable(True)          # event pairs around every GEMM launch in the graph
+    if args.no_graph:
+        planner.set_use_graphs(False)     # launch the graph's kernels one by one
     for _ in range(args.warmup):
         planner.plan(dz0, ds0, dgoal, dmu, dsg, B, H, N, K, R, wl.seed, out, stream=stream)
     planner.sync_check(stream)
     launches_per_step = planner.kernel_count(B, H, N, K, R)
 
-    # ---- device-resident timing (inputs already in HBM) ----
-    gemm_ms = gemm_flops = 0.0
-    gemm_launches = 0
+    # ---- device-resident timing (inputs already in HBM), plain graph replay ----
     barrier()
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -233,17 +232,31 @@ def run_ours(args, wl):
         ev0.record(stream)
         for _ in range(args.steps):
             planner.plan(dz0, ds0, dgoal, dmu, dsg, B, H, N, K, R, wl.seed, out, stream=stream)
-            stream.synchronize()
-            ms, fl, n = planner.profile_read()
-            gemm_ms += ms
-            gemm_flops += fl
-            gemm_launches += n
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
     planner.sync_check(stream)
     step_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
     clocks = clk.summary()
+
+    # ---- per-GEMM timing: a separately captured graph with event pairs around every GEMM
+    # (kept out of the timed region above: the event nodes add launch gaps) ----
+    gemm_ms = gemm_flops = 0.0
+    gemm_launches = 0
+    prof_steps = min(args.steps, 3)
+    if not args.no_graph:
+        planner.profile_enable(True)
+        planner.plan(dz0, ds0, dgoal, dmu, dsg, B, H, N, K, R, wl.seed, out, stream=stream)
+        stream.synchronize()
+        for _ in range(prof_steps):
+            planner.plan(dz0, ds0, dgoal, dmu, dsg, B, H, N, K, R, wl.seed, out, stream=stream)
+            stream.synchronize()
+            ms, fl, n = planner.profile_read()
+            gemm_ms += ms
+            gemm_flops += fl
+            gemm_launches += n
+        planner.profile_enable(False)
+        planner.sync_check(stream)
 
     # ---- end to end through the C ABI with pinned host buffers ----
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -283,7 +296,7 @@ def run_ours(args, wl):
         achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
         step_flops = None
         if gemm_launches:
-            step_flops = gemm_flops / args.steps
+            step_flops = gemm_flops / prof_steps
         line = {
             "metric": METRIC, "value": rollouts / (step_ms * 1e-3), "unit": "candidate rollouts/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -293,7 +306,9 @@ def run_ours(args, wl):
                        "parallelism": f"independent problems x{world} (no collective)",
                        "l2": "not flushed: working set (0.61 GB bf16 weights + ~4 GB activations "
                              "per round) exceeds the 129 MB L2",
-                       "timing": "CUDA events on the launch stream; host sync per step"},
+                       "timing": "CUDA events on the launch stream; host sync per step",
+                       "launch": "kernels launched one by one on the stream" if args.no_graph
+                                 else "one CUDA graph replay per step"},
             "roofline": {"bound": "tensor", "kernel": "k_gemm_tc (all predictor GEMMs)",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": (achieved / peak) if achieved else None,
@@ -301,7 +316,7 @@ def run_ours(args, wl):
                          "traffic": (sum(GEMM_DRAM_BYTES_PER_LAUNCH_FULL) / 4
                                      if args.workload == "full" and not args.candidates else None),
                          "traffic_unit": "DRAM bytes per launch (mean of the four per-layer GEMMs)",
-                         "gemm_share_of_step": (gemm_ms / args.steps) / step_ms if step_ms else None,
+                         "gemm_share_of_step": (gemm_ms / prof_steps) / step_ms if gemm_launches else None,
                          "gemm_tflop_per_step": step_flops / 1e12 if step_flops else None},
             "e2e": {"value": rollouts / (e2e_ms * 1e-3), "unit": "candidate rollouts/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -383,6 +398,9 @@ def main():
     ap.add_argument("--closed-loop", type=int, default=0, metavar="T",
                     help="time a T-step receding-horizon episode instead of one plan step")
     ap.add_argument("--warm", action="store_true", help="warm-start each step (--closed-loop)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the plan's kernels directly on the stream instead of replaying "
+                         "its CUDA graph (for the graph-vs-stream comparison)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -27,7 +27,8 @@ EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string
            "jepa_plan_kernel_count", "jepa_linear_bf16", "jepa_profile_enable",
            "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc",
            "jepa_attention_bf16", "jepa_cem_warm_start", "jepa_world_model_step",
-           "jepa_cem_closed_loop", "jepa_linear_fp8", "jepa_quantize_rows_fp8")
+           "jepa_cem_closed_loop", "jepa_linear_fp8", "jepa_quantize_rows_fp8",
+           "jepa_set_use_graphs")
 
 
 class JepaError(RuntimeError):
@@ -88,6 +89,7 @@ def load(path: str = _LIB_PATH):
         "jepa_cem_closed_loop": ([P, P, P, P, P, P, I, I, I, I, I, I, I, U64, P, P, P], I),
         "jepa_linear_fp8": ([P, P, P, P, P, P, I, I, I, I, P, P], I),
         "jepa_quantize_rows_fp8": ([P, P, I, I, P, P, P], I),
+        "jepa_set_use_graphs": ([P, I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -261,6 +263,9 @@ class Planner:
         self._check(self.lib.jepa_attention_bf16(self.h, _ptr(q), _ptr(kv), _ptr(out), ncand, T, Lk,
                                                  kv_rows, heads, d, _stream(stream)),
                     "attention_bf16")
+
+    def set_use_graphs(self, on: bool):
+        self._check(self.lib.jepa_set_use_graphs(self.h, int(on)), "set_use_graphs")
 
     def profile_enable(self, on: bool):
         self._check(self.lib.jepa_profile_enable(self.h, int(on)), "profile_enable")

@@ -66,15 +66,18 @@ struct Cfg {
 
 // 2-SM tiles: a CTA pair computes 256 x 256 (each CTA 128 rows, all 256 columns in its TMEM);
 // each CTA stages its own 128 rows of A and its own 128-row half of W per K step.
-template <int EW>
+template <int MODE>
 struct Cfg2 {
+  static constexpr int EW = epi_warps(MODE);
+  static constexpr int STG = stg_floats(MODE);
   static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
   static constexpr int B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of the 256 columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = EW > 8 ? 5 : 6;
+  static constexpr int FIT = (232448 - 1024 - 16 - 5 * 8 - EW * STG * 4) / (STAGE_BYTES + 16);
+  static constexpr int STAGES = FIT < 6 ? FIT : 6;
   static constexpr int TMEM_COLS = 512;         // two 256-column accumulators
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = STG_OFF + EW * STG_FLOATS * 4;
+  static constexpr int BAR_OFF = STG_OFF + EW * STG * 4;
   static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -616,7 +619,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
                int M, int N, int K, Epilogue epi, int* err_flag) {
   constexpr int EW = epi_warps(MODE);
   constexpr int BN = 256;
-  using C = Cfg2<EW>;
+  using C = Cfg2<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -733,7 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
   } else {
     // ---------------- epilogue (warps 2.., both CTAs) ----------------
     const int ew = warp - 2;
-    float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * STG_FLOATS;
+    float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * C::STG;
     int acc = 0;
     uint32_t acc_phase = 0;
     auto release = [](uint32_t bar) { mbar_arrive_cluster(bar); };
@@ -813,7 +816,7 @@ static cudaError_t launch_mode(const void* A, const void* W, int M, int N, int K
 template <int MODE, int OP>
 static cudaError_t launch_tc2(const void* A, const void* W, int M, int N, int K, const Epilogue& epi,
                               int* err_flag, int num_sms, cudaStream_t s) {
-  using C = Cfg2<epi_warps(MODE)>;
+  using C = Cfg2<MODE>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2<MODE, OP>,

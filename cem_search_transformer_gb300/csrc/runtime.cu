@@ -89,6 +89,7 @@ struct jepa_ctx {
   int* dev_err = nullptr;
   cudaStream_t cap_stream = nullptr;
   bool profile = false;
+  bool use_graphs = true;   // false: jepa_cem_plan launches the graph's kernels on the stream
   PlanGraph* last_plan = nullptr;
   // closed-loop episode state (grow-only; see jepa_cem_closed_loop)
   std::vector<void*> ep_allocs;
@@ -423,6 +424,31 @@ jepa_status check_ready(jepa_ctx* ctx) {
   return JEPA_OK;
 }
 
+// The kernels of one planning step (all rounds), enqueued on s: captured once into the
+// plan's graph, or launched directly when graphs are switched off.
+jepa_status plan_body(jepa_ctx* ctx, PlanGraph* g, cudaStream_t s, PlanGraph* prof) {
+  const int B = g->B, H = g->H, N = g->N, K = g->K, R = g->R;
+  const int A = ctx->cfg.action_dim, HA = H * A;
+  const size_t BN = (size_t)B * N;
+  jepa_status s2;
+  if ((s2 = context_projection(ctx, g->z0, g->z0_act, g->base, B, s, prof))) return s2;
+  for (int r = 0; r < R; ++r) {
+    float* act_r = g->actions + (size_t)r * BN * HA;
+    float* en_r = g->energy + (size_t)r * BN;
+    CK(sample_actions(g->mu + (size_t)r * B * HA, g->sigma + (size_t)r * B * HA, B, N, H, A, r,
+                      g->seed, 0, act_r, s));
+    if ((s2 = predictor_pass(ctx, g->base, g->state0, act_r, B, N, H, g->goal, nullptr, en_r,
+                             s, prof)))
+      return s2;
+    CK(select_refit(en_r, act_r, B, N, HA, K, g->mu + (size_t)(r + 1) * B * HA,
+                    g->sigma + (size_t)(r + 1) * B * HA, g->elites + (size_t)r * B * K,
+                    g->winner, s));
+  }
+  CK(winner_action(g->actions + (size_t)(R - 1) * BN * HA, g->winner, B, N, HA, A,
+                   g->action_out, s));
+  return JEPA_OK;
+}
+
 jepa_status build_plan(jepa_ctx* ctx, int B, int H, int N, int K, int R, PlanGraph** out) {
   const auto key = std::make_tuple(B, H, N, K, R, ctx->profile);
   auto it = ctx->graphs.find(key);
@@ -457,29 +483,11 @@ jepa_status build_plan(jepa_ctx* ctx, int B, int H, int N, int K, int R, PlanGra
   PlanGraph* prof = ctx->profile ? g : nullptr;
   cudaStream_t s = ctx->cap_stream;
   cudaError_t ce = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  auto body = [&]() { return plan_body(ctx, g, s, prof); };
   if (ce != cudaSuccess) {
     free_plan(g);
     return fail(ctx, JEPA_ERR_CUDA, "begin capture: %s", cudaGetErrorString(ce));
   }
-  auto body = [&]() -> jepa_status {
-    jepa_status s2;
-    if ((s2 = context_projection(ctx, g->z0, g->z0_act, g->base, B, s, prof))) return s2;
-    for (int r = 0; r < R; ++r) {
-      float* act_r = g->actions + (size_t)r * BN * HA;
-      float* en_r = g->energy + (size_t)r * BN;
-      CK(sample_actions(g->mu + (size_t)r * B * HA, g->sigma + (size_t)r * B * HA, B, N, H, A, r,
-                        g->seed, 0, act_r, s));
-      if ((s2 = predictor_pass(ctx, g->base, g->state0, act_r, B, N, H, g->goal, nullptr, en_r,
-                               s, prof)))
-        return s2;
-      CK(select_refit(en_r, act_r, B, N, HA, K, g->mu + (size_t)(r + 1) * B * HA,
-                      g->sigma + (size_t)(r + 1) * B * HA, g->elites + (size_t)r * B * K,
-                      g->winner, s));
-    }
-    CK(winner_action(g->actions + (size_t)(R - 1) * BN * HA, g->winner, B, N, HA, A,
-                     g->action_out, s));
-    return JEPA_OK;
-  };
   st = body();
   cudaGraph_t graph = nullptr;
   ce = cudaStreamEndCapture(s, &graph);
@@ -893,7 +901,11 @@ jepa_status jepa_cem_plan(jepa_ctx* ctx, const float* z0, const float* state0, c
   CK(cudaMemcpyAsync(g->mu, mu0, B * HA * 4, cudaMemcpyDefault, s));
   CK(cudaMemcpyAsync(g->sigma, sigma0, B * HA * 4, cudaMemcpyDefault, s));
   CK(set_u64(g->seed, seed, s));
-  CK(cudaGraphLaunch(g->exec, s));
+  if (ctx->use_graphs) {
+    CK(cudaGraphLaunch(g->exec, s));
+  } else if ((st = plan_body(ctx, g, s, nullptr))) {
+    return st;
+  }
   CK(cudaMemcpyAsync(action_out, g->action_out, (size_t)B * c.action_dim * 4, cudaMemcpyDefault, s));
   if (trace) {
     const size_t BN = (size_t)B * N, R = rounds;
@@ -1099,6 +1111,12 @@ jepa_status jepa_attention_bf16(jepa_ctx* ctx, const uint16_t* q, const uint16_t
   cudaStream_t s = (cudaStream_t)stream;
   CK(attention_tc_bf16((const bf16*)q, (const bf16*)kv, (bf16*)out, ncand, T, Lk, kv_rows, heads, d,
                        ctx->dev_err, s));
+  return JEPA_OK;
+}
+
+jepa_status jepa_set_use_graphs(jepa_ctx* ctx, int enable) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  ctx->use_graphs = enable != 0;
   return JEPA_OK;
 }
 

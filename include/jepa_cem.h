@@ -259,6 +259,11 @@ jepa_status jepa_attention_bf16(jepa_ctx* ctx, const uint16_t* q, const uint16_t
                                 int ncand, int T, int Lk, int kv_rows, int heads, int d,
                                 void* stream);
 
+/* enable = 0: jepa_cem_plan launches the kernels of its captured graph one by one on the
+ * stream instead of replaying the graph (same kernels, same results; for measuring what the
+ * graph saves). enable != 0 (the default): graph replay. */
+jepa_status jepa_set_use_graphs(jepa_ctx* ctx, int enable);
+
 /* Kernel-level timing of the predictor GEMMs inside plan graphs. enable != 0 makes graphs
  * captured afterwards record a CUDA event pair around every GEMM launch (graphs captured
  * before keep their state). jepa_profile_read (after the stream is synchronised) returns
