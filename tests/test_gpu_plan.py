@@ -181,3 +181,19 @@ def test_small_gated_plan_teacher_forced():
                     sample=range(0, 200, 23))
     assert np.array_equal(out[0], tr["actions"][-1, 0][tr["winner"][0], 0])
     p.close()
+
+
+def test_plan_without_graph_is_bitwise_identical():
+    """Launching the plan's kernels one by one (graphs off) gives the graph replay's result."""
+    wl = synthetic.WORKLOADS["small"]
+    pc = wl.predictor
+    p = make_planner("small", max_horizon=wl.horizon)
+    z0, goal, s0 = synthetic.make_problems(pc, 1)
+    mu0, sg0 = synthetic.make_gaussian(pc, 1, wl.horizon)
+    out_g, tr_g = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    p.set_use_graphs(False)
+    out_s, tr_s = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    assert np.array_equal(out_g, out_s)
+    for k in tr_g:
+        assert np.array_equal(tr_g[k], tr_s[k]), k
+    p.close()
