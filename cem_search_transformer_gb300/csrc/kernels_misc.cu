@@ -223,6 +223,78 @@ __global__ void k_layernorm(const float* __restrict__ x, RowMap in_map, void* __
   }
 }
 
+// The same LayerNorm for widths that are a multiple of 128: lane l holds columns
+// 128 i + 4 l .. + 3 (i < G = d / 128), so every load is a 16-byte vector and every warp
+// instruction moves 512 contiguous bytes.
+template <int G, int OUT>
+__global__ void k_layernorm_v4(const float* __restrict__ x, RowMap in_map, void* __restrict__ y,
+                               float* __restrict__ yscale, const float* __restrict__ g,
+                               const float* __restrict__ bta, int rows, float eps) {
+  constexpr int D = 128 * G;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + map_row(in_map, warp) * D) + lane;
+  float4 v[G];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    v[i] = __ldcs(xr + 32 * i);
+    s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s * (1.0f / D);
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, e = v[i].w - mean;
+    q += (a * a + b * b) + (c * c + e * e);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  const float rstd = rsqrtf(q * (1.0f / D) + eps);
+  const float4* g4 = reinterpret_cast<const float4*>(g) + lane;
+  const float4* b4 = reinterpret_cast<const float4*>(bta) + lane;
+#pragma unroll
+  for (int i = 0; i < G; ++i) {
+    const float4 gg = __ldg(g4 + 32 * i), bb = __ldg(b4 + 32 * i);
+    v[i] = make_float4((v[i].x - mean) * rstd * gg.x + bb.x, (v[i].y - mean) * rstd * gg.y + bb.y,
+                       (v[i].z - mean) * rstd * gg.z + bb.z, (v[i].w - mean) * rstd * gg.w + bb.w);
+  }
+  const long long base = (long long)warp * D + 4 * lane;
+  if constexpr (OUT == 2) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float inv = amax > 0.f ? 448.f / amax : 1.f;
+    if (lane == 0) yscale[warp] = amax > 0.f ? amax / 448.f : 1.f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const uint32_t w = (uint32_t)e4m3_code(v[i].x * inv) | ((uint32_t)e4m3_code(v[i].y * inv) << 8) |
+                         ((uint32_t)e4m3_code(v[i].z * inv) << 16) | ((uint32_t)e4m3_code(v[i].w * inv) << 24);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(y) + base + 128 * i) = w;
+    }
+  } else if constexpr (OUT == 1) {
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v[i].x, v[i].y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(v[i].z, v[i].w);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(reinterpret_cast<bf16*>(y) + base + 128 * i) = u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(y) + base + 128 * i) = v[i];
+  }
+}
+
 // Per-row fp8 quantisation of fp32 rows (weights at load time, and the C ABI): one warp per
 // row, the same scale rule and rounding as the LayerNorm's fp8 output.
 __global__ void k_quantize_rows(const float* __restrict__ src, long long rows, int cols,
@@ -265,11 +337,34 @@ static cudaError_t launch_ln(const float* x, RowMap m, void* y, float* yscale, i
   return cudaGetLastError();
 }
 
+template <int G>
+static cudaError_t launch_ln4(const float* x, RowMap m, void* y, float* yscale, int out_kind,
+                              const float* g, const float* b, int rows, float eps, cudaStream_t s) {
+  const int threads = 256;
+  const unsigned blocks = (unsigned)(((long long)rows * 32 + threads - 1) / threads);
+  if (out_kind == 2)
+    k_layernorm_v4<G, 2><<<blocks, threads, 0, s>>>(x, m, y, yscale, g, b, rows, eps);
+  else if (out_kind == 1)
+    k_layernorm_v4<G, 1><<<blocks, threads, 0, s>>>(x, m, y, yscale, g, b, rows, eps);
+  else
+    k_layernorm_v4<G, 0><<<blocks, threads, 0, s>>>(x, m, y, yscale, g, b, rows, eps);
+  return cudaGetLastError();
+}
+
 cudaError_t layernorm(const float* x, RowMap in_map, void* y, int out_kind, const float* g,
                       const float* b, int rows, int d, float eps, cudaStream_t s,
                       float* yscale) {
   if (rows <= 0) return cudaSuccess;
   if (out_kind == 2 && !yscale) return cudaErrorInvalidValue;
+  switch (d) {   // widths of the predictor configurations: 16-byte vector path
+    case 128: return launch_ln4<1>(x, in_map, y, yscale, out_kind, g, b, rows, eps, s);
+    case 384: return launch_ln4<3>(x, in_map, y, yscale, out_kind, g, b, rows, eps, s);
+    case 512: return launch_ln4<4>(x, in_map, y, yscale, out_kind, g, b, rows, eps, s);
+    case 768: return launch_ln4<6>(x, in_map, y, yscale, out_kind, g, b, rows, eps, s);
+    case 1024: return launch_ln4<8>(x, in_map, y, yscale, out_kind, g, b, rows, eps, s);
+    case 2048: return launch_ln4<16>(x, in_map, y, yscale, out_kind, g, b, rows, eps, s);
+    default: break;
+  }
   if (d <= 128) return launch_ln<4>(x, in_map, y, yscale, out_kind, g, b, rows, d, eps, s);
   if (d <= 512) return launch_ln<16>(x, in_map, y, yscale, out_kind, g, b, rows, d, eps, s);
   if (d <= 1024) return launch_ln<32>(x, in_map, y, yscale, out_kind, g, b, rows, d, eps, s);
