@@ -29,7 +29,8 @@ def _from_bits(b):
                                                       (130, 2, 2, 3), (66, 2, 6, 2),
                                                       (256, 1, 1, 1), (300, 1, 2, 1),
                                                       (129, 2, 3, 2), (387, 1, 2, 2),
-                                                      (387, 2, 1, 1)])
+                                                      (387, 2, 1, 1), (263, 1, 2, 3),
+                                                      (136, 2, 3, 2)])
 def test_attention_matches_oracle(planner, T, Lk_blocks, heads, ncand):
     d = heads * 64
     kv_rows = 3 * T
