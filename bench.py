@@ -51,6 +51,23 @@ def load_peaks():
     return PEAK_FALLBACK, "fallback"
 
 
+def rank_problems(pc, B, rank):
+    """Weak scaling by independent problems: rank r plans problems r*B .. r*B + B - 1 (the
+    same seeded inputs a single process would draw for them)."""
+    return synthetic.make_problems(pc, B, seed_base=1000 + rank * B)
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Max over ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def rank_info():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -199,7 +216,7 @@ def run_ours(args, wl):
     planner = binding.Planner(pc, max_horizon=H, device=local)
     planner.load_weights(synthetic.make_weights(pc, seed=0))
     # each rank plans its own problems (independent units, weak scaling)
-    z0, goal, s0 = synthetic.make_problems(pc, B, seed_base=1000 + rank * B)
+    z0, goal, s0 = rank_problems(pc, B, rank)
     mu0, sg0 = synthetic.make_gaussian(pc, B, H)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     dz0, dgoal, ds0, dmu, dsg = t(z0), t(goal), t(s0), t(mu0), t(sg0)
@@ -211,11 +228,7 @@ def run_ours(args, wl):
             dist.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        tt = torch.tensor([x], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        return float(tt.item())
+        return reduce_max(x, world, dev)
 
     if args.no_graph:
         planner.set_use_graphs(False)     # launch the graph's kernels one by one
