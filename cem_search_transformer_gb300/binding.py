@@ -28,7 +28,7 @@ EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string
            "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc",
            "jepa_attention_bf16", "jepa_cem_warm_start", "jepa_world_model_step",
            "jepa_cem_closed_loop", "jepa_linear_fp8", "jepa_quantize_rows_fp8",
-           "jepa_set_use_graphs")
+           "jepa_set_use_graphs", "jepa_selftest_bounded_wait")
 
 
 class JepaError(RuntimeError):
@@ -90,6 +90,7 @@ def load(path: str = _LIB_PATH):
         "jepa_linear_fp8": ([P, P, P, P, P, P, I, I, I, I, P, P], I),
         "jepa_quantize_rows_fp8": ([P, P, I, I, P, P, P], I),
         "jepa_set_use_graphs": ([P, I], I),
+        "jepa_selftest_bounded_wait": ([P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -275,6 +276,10 @@ class Planner:
         self._check(self.lib.jepa_profile_read(self.h, ctypes.byref(ms), ctypes.byref(fl),
                                                ctypes.byref(n)), "profile_read")
         return ms.value, fl.value, n.value
+
+    def selftest_bounded_wait(self, stream=None):
+        self._check(self.lib.jepa_selftest_bounded_wait(self.h, _stream(stream)),
+                    "selftest_bounded_wait")
 
     def sync_check(self, stream=None):
         self._check(self.lib.jepa_sync_check(self.h, _stream(stream)), "sync_check")

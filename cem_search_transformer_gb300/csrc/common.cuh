@@ -296,6 +296,7 @@ cudaError_t set_u64(uint64_t* p, uint64_t v, cudaStream_t s);
 cudaError_t warm_start(const float* mu_prev, const float* mu_prior, const float* sigma_prior, int B,
                        int H, int A, float* mu_out, float* sigma_out, cudaStream_t s);
 cudaError_t state_step(const float* st, const float* a, int n, float* s_out, cudaStream_t s);
+cudaError_t wait_selftest(int* err_flag, cudaStream_t s);
 
 // fp32 -> bf16 (round to nearest even)
 cudaError_t convert_f32_bf16(const float* x, bf16* y, long long n, cudaStream_t s);

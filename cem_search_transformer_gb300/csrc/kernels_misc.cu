@@ -5,6 +5,7 @@
 // "Where the sixteen seconds actually goes" (draw candidates from a Gaussian, score
 // against the goal, keep the best K, re-centre the Gaussian).
 #include "common.cuh"
+#include "tc_common.cuh"
 
 #include <float.h>
 
@@ -713,6 +714,24 @@ cudaError_t attention_f32(const float* q, const float* kv, float* o, int ncand, 
   const float scale = 1.0f / sqrtf((float)(d / heads));
   k_attention_f32<<<grid, FA32_WARPS * 32, smem, s>>>(q, kv, o, T, Lk, kv_cand_stride_rows, heads, d,
                                                        scale);
+  return cudaGetLastError();
+}
+
+// Failure-detection self-test: one thread waits on an mbarrier that nothing arrives on,
+// through the same bounded wait every pipelined kernel uses; after its limit the wait gives
+// up, raises the context's error flag and the kernel returns (no fault, no hang).
+__global__ void k_wait_selftest(int* err_flag) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = tc::smem_u32(&bar);
+  tc::mbar_init(b, 1);
+  abort_flag = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  tc::mbar_wait(b, 0, &abort_flag, err_flag);
+}
+
+cudaError_t wait_selftest(int* err_flag, cudaStream_t s) {
+  k_wait_selftest<<<1, 1, 0, s>>>(err_flag);
   return cudaGetLastError();
 }
 

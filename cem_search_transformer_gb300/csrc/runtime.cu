@@ -1144,6 +1144,13 @@ jepa_status jepa_profile_read(jepa_ctx* ctx, double* gemm_ms, double* gemm_flops
   return JEPA_OK;
 }
 
+jepa_status jepa_selftest_bounded_wait(jepa_ctx* ctx, void* stream) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  CK(cudaSetDevice(ctx->device));
+  CK(wait_selftest(ctx->dev_err, (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
 jepa_status jepa_sync_check(jepa_ctx* ctx, void* stream) {
   if (!ctx) return JEPA_ERR_INVALID_ARG;
   CK(cudaSetDevice(ctx->device));

@@ -294,6 +294,13 @@ jepa_status jepa_profile_read(jepa_ctx* ctx, double* gemm_ms, double* gemm_flops
 jepa_status jepa_energy_l1_noalloc(const float* z_pred, const float* goal, int B, int N, int P,
                                    int E, float* energy, void* stream, char* err, size_t err_len);
 
+/* Failure-detection self-test: launches one thread that waits, through the bounded mbarrier
+ * wait every pipelined kernel of this library uses, on a barrier nothing will arrive on.
+ * After the wait's limit (2 s) it gives up, raises this context's error flag and returns;
+ * the next jepa_sync_check then reports JEPA_ERR_TIMEOUT (and clears the flag). Nothing
+ * faults or hangs; the context stays usable. */
+jepa_status jepa_selftest_bounded_wait(jepa_ctx* ctx, void* stream);
+
 /* Synchronise `stream`, then report JEPA_ERR_TIMEOUT if a bounded device-side wait in
  * any kernel of this context gave up since the last check (the flag is then cleared). */
 jepa_status jepa_sync_check(jepa_ctx* ctx, void* stream);
