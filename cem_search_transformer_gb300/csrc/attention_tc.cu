@@ -10,17 +10,23 @@
 // Persistent: each CTA walks work items (128-query tile, head, candidate), tile fastest so
 // that the CTAs working on one candidate's K/V at the same time share it in L2. 6 warps:
 //   warp 0      TMA producer: for each item its Q tile (double-buffered) and its 64-key K and
-//               V chunks through a 3-stage ring. It runs ahead across item boundaries, so
+//               V chunks through a 4-stage ring. It runs ahead across item boundaries, so
 //               the next item's loads hide behind the current item's math;
 //   warp 1      TMEM allocator and single-thread MMA issuer:
 //                 S = Q K^T   (M 128, N 64, K 64; both operands K-major, 128B-swizzled)
-//                 O += P V    (M 128, N 64, K 64; P K-major from shared memory, V read
-//                              MN-major straight from its TMA tile)
+//                 O += P V    (M 128, N 64, K 64; P read from TMEM, V read MN-major
+//                              straight from its TMA tile)
+//               Chunk g's scores go to S buffer g % 2; the scores of chunk g + 2 are issued
+//               right after P V of chunk g, which has consumed that buffer;
 //   warps 2-5   softmax, one query row per thread: read S from TMEM, online max / sum,
-//               write P (bf16, 128B-swizzled) to shared memory, rescale O in TMEM, and at the
-//               end of an item normalise O and store it.
-// TMEM: S in columns [0, 64), O of even items in [64, 128), of odd items in [128, 192), so
-// one item's output read-out overlaps the next item's MMAs. Keys past Lk are masked to
+//               write P (bf16, two per column) over the first 32 columns of the same S
+//               buffer, rescale O in TMEM, and at the end of an item normalise O and store it.
+//               The exponentials of chunk g overlap P V of chunk g - 1: only the O rescale
+//               (rare, see below) and the hand-over of P wait for it.
+// TMEM: S / P buffers in columns [0, 64) and [192, 256), O of even items in [64, 128), of
+// odd items in [128, 192), so one item's output read-out overlaps the next item's MMAs.
+// In a partial last tile the rows of inactive warps keep stale words in P; their O rows
+// are computed from them but never read. Keys past Lk are masked to
 // -inf (their P is 0; the K/V rows loaded there are finite: cache rows are zero-initialised
 // or belong to a neighbouring candidate, and rows past the tensor read as zero). In the last
 // tile of a block whose T is not a multiple of 128, warps whose rows all lie past T skip the
@@ -38,18 +44,16 @@ constexpr int AQ = 128;    // query rows per item (MMA M)
 constexpr int AK = 64;     // keys per chunk
 constexpr int AHD = 64;    // head dim
 constexpr int A_THREADS = 192;
-constexpr int KV_STAGES = 3;
+constexpr int KV_STAGES = 4;
 constexpr int Q_BYTES = AQ * AHD * 2;     // 16 KB
 constexpr int KV_BYTES = AK * AHD * 2;    // 8 KB (K or V chunk)
-constexpr int P_BYTES = AQ * AK * 2;      // 16 KB
 constexpr int OFF_Q = 0;                  // two Q buffers
 constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
 constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
-constexpr int OFF_P = OFF_V + KV_STAGES * KV_BYTES;
-constexpr int OFF_BAR = OFF_P + P_BYTES;
-// q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full, s_free, p_full, o_full,
-// o_free[2], teardown
-constexpr int NUM_BARS = 4 + 2 * KV_STAGES + 4 + 2 + 1;
+constexpr int OFF_BAR = OFF_V + KV_STAGES * KV_BYTES;
+// q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full, o_full, o_free[2],
+// teardown
+constexpr int NUM_BARS = 4 + 2 * KV_STAGES + 2 + 2 + 2 + 1;
 constexpr int A_SMEM = OFF_BAR + NUM_BARS * 8 + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr int CTAS_PER_SM = 2;
@@ -74,10 +78,11 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
   auto q_empty = [&](int b) { return bar + 8u * (2 + b); };
   auto kv_full = [&](int s) { return bar + 8u * (4 + s); };
   auto kv_empty = [&](int s) { return bar + 8u * (4 + KV_STAGES + s); };
-  const uint32_t s_full = bar + 8u * (4 + 2 * KV_STAGES), s_free = s_full + 8, p_full = s_full + 16,
-                 o_full = s_full + 24;
-  auto o_free = [&](int b) { return s_full + 32 + 8u * b; };
-  const uint32_t teardown = s_full + 48;
+  const uint32_t s_full0 = bar + 8u * (4 + 2 * KV_STAGES);
+  auto s_full = [&](int b) { return s_full0 + 8u * b; };
+  const uint32_t p_full = s_full0 + 16, o_full = s_full0 + 24;
+  auto o_free = [&](int b) { return s_full0 + 32 + 8u * b; };
+  const uint32_t teardown = s_full0 + 48;
   uint32_t* tmem_slot = (uint32_t*)(smem + OFF_BAR + NUM_BARS * 8);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
@@ -103,8 +108,8 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 4);
+    mbar_init(s_full(0), 1);
+    mbar_init(s_full(1), 1);
     mbar_init(p_full, 4);
     mbar_init(o_full, 1);
     mbar_init(teardown, 1);
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;
+  auto tS = [&](int g) { return tmem + ((g & 1) ? 192u : 0u); };   // S / P buffer of chunk g
   auto tO = [&](int i) { return tmem + 64u + 64u * (uint32_t)(i & 1); };
 
   if (warp == 0) {
@@ -164,41 +169,45 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         const uint64_t qdesc = desc_sw128(sb + OFF_Q + (ii & 1) * Q_BYTES);
         const uint64_t kdesc = desc_sw128(sb + OFF_K + (gg % KV_STAGES) * KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < AHD / 16; ++kk) mma_bf16_ss(tS, qdesc + 2 * kk, kdesc + 2 * kk, idS, kk > 0);
-        mma_commit(s_full);
+        for (int kk = 0; kk < AHD / 16; ++kk)
+          mma_bf16_ss(tS(gg), qdesc + 2 * kk, kdesc + 2 * kk, idS, kk > 0);
+        mma_commit(s_full(gg & 1));
       };
       auto ready_s = [&](int gg) {   // operands of S for chunk gg are in shared memory
         const int ii = gg / nch;
         if (gg % nch == 0 && !mbar_wait(q_full(ii & 1), (ii >> 1) & 1, abort_flag, err_flag)) return false;
         return mbar_wait(kv_full(gg % KV_STAGES), (gg / KV_STAGES) & 1, abort_flag, err_flag);
       };
-      bool ok = total > 0 && ready_s(0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
+      bool ok = true;
+      for (int gg = 0; gg < 2 && gg < total && ok; ++gg) {
+        ok = ready_s(gg);
+        if (ok) {
+          tc_fence_after();
+          issue_s(gg);
+        }
       }
       for (int gg = 0; gg < total && ok; ++gg) {
         const int ii = gg / nch, j = gg % nch;
-        if (gg + 1 < total) {
-          // S is single-buffered: the next chunk's scores go in once the softmax has read S
-          if (!ready_s(gg + 1) || !mbar_wait(s_free, gg & 1, abort_flag, err_flag)) break;
-          tc_fence_after();
-          issue_s(gg + 1);
-        }
         if (!mbar_wait(p_full, gg & 1, abort_flag, err_flag)) break;
         // the O buffer of this item was last read out for item ii - 2
         if (j == 0 && ii >= 2 && !mbar_wait(o_free(ii & 1), ((ii >> 1) - 1) & 1, abort_flag, err_flag))
           break;
         tc_fence_after();
-        const uint64_t pdesc = desc_sw128(sb + OFF_P);
         const uint64_t vdesc = desc_sw128_mn(sb + OFF_V + (gg % KV_STAGES) * KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < AK / 16; ++kk)  // 16 keys = 16 rows x 128 B = 2048 B per step
-          mma_bf16_ss(tO(ii), pdesc + 2 * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), idO,
+        for (int kk = 0; kk < AK / 16; ++kk)  // 16 keys: 8 TMEM columns of P, 16 rows x 128 B of V
+          mma_bf16_ts(tO(ii), tS(gg) + 8u * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), idO,
                       (j > 0) || (kk > 0));
         mma_commit(o_full);
         mma_commit(kv_empty(gg % KV_STAGES));
         if (j == nch - 1) mma_commit(q_empty(ii & 1));
+        // tensor-core operations of this thread run in issue order, so the scores of chunk
+        // gg + 2 overwrite this S / P buffer only after the P V above has read it
+        if (gg + 2 < total) {
+          if (!ready_s(gg + 2)) break;
+          tc_fence_after();
+          issue_s(gg + 2);
+        }
       }
       mma_commit(teardown);
       const unsigned long long t0 = globaltimer();
@@ -221,31 +230,27 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
       const uint32_t tOi = tO(i);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nch; ++j, ++g) {
-        if (!mbar_wait(s_full, g & 1, abort_flag, err_flag)) {
+        const uint32_t tSg = tS(g);
+        if (!mbar_wait(s_full(g & 1), (g >> 1) & 1, abort_flag, err_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (!active) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_free);
           if (j > 0 && !mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
             ok = false;
             break;
           }
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(p_full);
           continue;
         }
         uint32_t sa[32], sc[32];
-        tmem_ld32_async(tS + lane_off, sa);
-        tmem_ld32_async(tS + lane_off + 32, sc);
+        tmem_ld32_async(tSg + lane_off, sa);
+        tmem_ld32_async(tSg + lane_off + 32, sc);
         tmem_wait(sa);
         tmem_wait(sc);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
         float s[64];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -274,17 +279,8 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         const float mnew = bump ? fmaxf(m, cmax) : m;
         const float alpha = ex2f((m - mnew) * scale_log2);   // 1 when m is kept, 0 at j = 0
         const float ms = mnew * scale_log2;
-        // the previous P V must be complete before P is overwritten and O is rescaled
-        if (j > 0) {
-          if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        // exponentiate, sum and store P 8 columns (16 bytes) at a time: 64 bf16 per row,
-        // chunk cc of the 128-byte row stored at position cc ^ (row % 8) (128-byte swizzle)
-        uint8_t* prow = smem + OFF_P + (row >> 3) * 1024 + (row & 7) * 128;
+        // exponentiate and sum, packing P as bf16 pairs (key 2c in the low half of column c)
+        uint32_t pk[32];
         float rsp[8];
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
@@ -298,20 +294,25 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
             for (int t = 0; t < 8; ++t) e[t] = ex2f(fmaf(s[8 * cc + t], scale_log2, -ms));
           }
           rsp[cc] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(e[0], e[1]);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(e[2], e[3]);
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(e[4], e[5]);
-          __nv_bfloat162 p3 = __floats2bfloat162_rn(e[6], e[7]);
-          uint4 u;
-          u.x = *reinterpret_cast<uint32_t*>(&p0);
-          u.y = *reinterpret_cast<uint32_t*>(&p1);
-          u.z = *reinterpret_cast<uint32_t*>(&p2);
-          u.w = *reinterpret_cast<uint32_t*>(&p3);
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) = u;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            __nv_bfloat162 pp = __floats2bfloat162_rn(e[2 * t], e[2 * t + 1]);
+            pk[4 * cc + t] = *reinterpret_cast<uint32_t*>(&pp);
+          }
         }
+        // S of this chunk is in registers: P takes its first 32 columns
+        tmem_st32(tSg + lane_off, pk);
         const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
         l = l * alpha + rs;
         m = mnew;
+        // P V of the previous chunk must be complete before O is rescaled and P handed over
+        if (j > 0) {
+          if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
           uint32_t ov[32], ow[32];
           tmem_ld32_async(tOi + lane_off, ov);
@@ -325,9 +326,8 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
           }
           tmem_st32(tOi + lane_off, ov);
           tmem_st32(tOi + lane_off + 32, ow);
-          tmem_st_wait();
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the MMA
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
