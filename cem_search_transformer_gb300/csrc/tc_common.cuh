@@ -44,10 +44,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait. Returns false (after raising the abort flags) when the limit expires or
-// another role already aborted.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_smem,
-                                       int* err_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+// another role already aborted. The first probe is inlined; the polling loop is not.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort_smem, int* err_flag) {
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -60,6 +59,10 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_smem,
+                                          int* err_flag) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_smem, err_flag);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
