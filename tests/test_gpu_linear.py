@@ -24,6 +24,8 @@ def _bf16_bits(x):
                                         (1000, 512, 1024, 1),    # BN=256 path, GELU
                                         (129, 1408, 64, 0),      # one K block, 11 N tiles
                                         (4096, 3072, 1024, 0),   # QKV shape, many tiles
+                                        (4100, 1536, 384, 1),    # GELU on CTA pairs, ragged M,
+                                                                 # both accumulators
                                         (77, 256, 4096, 1)])     # long K
 def test_linear_bf16_matches_matmul(planner, M, N, K, gelu):
     rng = np.random.default_rng(M + N + K)
