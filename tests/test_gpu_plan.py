@@ -111,6 +111,46 @@ def test_full_shape_plan_teacher_forced():
     p.close()
 
 
+def test_sweep_batched_full_shape_teacher_forced():
+    """A throughput-sweep cell at the full shape: B = 4 problems of N = 400 candidates share
+    one candidate axis of 1600 rollouts, cut into chunks of 1024, so a chunk boundary falls
+    inside problem 2 (between its candidates 223 and 224). Every problem is checked round by
+    round against the oracle (sampler, elites, refit), sampled energies on both sides of the
+    boundary, and problem 2's rollouts run as a chunk of their own give the same energies
+    bit for bit."""
+    wl = synthetic.WORKLOADS["sweep_N400_B4"]
+    pc = wl.predictor
+    B, N, K, R = wl.B, wl.N, wl.K, wl.rounds
+    p = make_planner("full", max_horizon=1)
+    z0, goal, s0 = synthetic.make_problems(pc, B)
+    mu0, sg0 = synthetic.make_gaussian(pc, B, 1)
+    out, tr = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    for b in range(B):
+        for r in range(R):
+            a_ref = philox.sample_actions(tr["mu"][r, b], tr["sigma"][r, b],
+                                          philox.sample_eps(wl.seed, b, r, N, 1, 7))
+            assert np.max(np.abs(tr["actions"][r, b] - a_ref)) < TOL_EPS
+            el = cem.select_elites(tr["energy"][r, b], K)
+            assert np.array_equal(el, tr["elites"][r, b])
+            m_ref, s_ref = cem.refit(tr["actions"][r, b][el])
+            assert np.max(np.abs(tr["mu"][r + 1, b] - m_ref)) < TOL_REFIT
+            assert np.max(np.abs(tr["sigma"][r + 1, b] - s_ref)) < TOL_REFIT
+        assert tr["winner"][b] == tr["elites"][-1, b][0]
+        assert np.array_equal(out[b], tr["actions"][-1, b][tr["winner"][b], 0])
+    w = oracle_weights_for("full")
+    for b, r, n in ((0, 0, 3), (2, 0, 223), (2, 0, 224), (3, R - 1, int(tr["winner"][3]))):
+        z = predictor.rollout(w, pc, z0[b], s0[b], tr["actions"][r, b][[n]].astype(np.float64))[-1]
+        assert rel_err(tr["energy"][r, b][[n]], predictor.energy_l1(z, goal[b])) < TOL_BF16_ENERGY_REL
+    # problem 2's round-0 rollouts on their own (one chunk of 400 instead of straddling two
+    # chunks of the batch) give the same energies bit for bit
+    en = torch.zeros(1, N, device="cuda")
+    p.predictor_forward(cuda(z0[2:3]), cuda(s0[2:3]), cuda(tr["actions"][0, 2:3]), 1, N, 1,
+                        goal=cuda(goal[2:3]), energy=en)
+    p.sync_check()
+    assert np.array_equal(host(en)[0], tr["energy"][0, 2])
+    p.close()
+
+
 def test_plan_batching_and_host_buffers():
     """B problems planned together equal each planned alone (bitwise), and host buffers give
     the same answer as device buffers."""
