@@ -134,6 +134,9 @@ def weight_shapes(cfg: PredictorConfig) -> Dict[str, tuple]:
     return shapes
 
 
+LN_GAINS = ("ln1_g", "ln2_g", "lnf_g")
+
+
 def make_weights(cfg: PredictorConfig, seed: int = 0, std: float = 0.02) -> Dict[str, np.ndarray]:
     """Random-init predictor weights (fp32), drawn in canonical order from one stream."""
     rng = np.random.default_rng(seed)
@@ -141,7 +144,7 @@ def make_weights(cfg: PredictorConfig, seed: int = 0, std: float = 0.02) -> Dict
     out: Dict[str, np.ndarray] = {}
     for name in weight_names(cfg):
         w = rng.standard_normal(shapes[name], dtype=np.float32) * np.float32(std)
-        if name.endswith("_g"):
+        if name.split(".")[-1] in LN_GAINS:          # LayerNorm gains near 1
             w = w + np.float32(1.0)
         out[name] = w.astype(np.float32)
     return out

@@ -124,26 +124,11 @@ def test_forward_argument_errors():
     p.close()
 
 
-def _ln_rounding_effect(monkeypatch, name, pc, z0, s0, acts, z_ref):
-    """How far the fp64 oracle's frame moves when only its LayerNorm outputs are rounded to
-    bf16 (one of the roundings the bf16 path makes): the scale of activation-rounding error
-    this network amplifies."""
-    ln = predictor.layer_norm
-    monkeypatch.setattr(predictor, "layer_norm", lambda x, g, b, eps: predictor.round_to_bf16(
-        np.asarray(ln(x, g, b, eps), np.float32)).astype(np.float64))
-    z_emu = predictor.rollout(oracle_weights_for(name), pc, z0, s0, acts.astype(np.float64))[-1]
-    monkeypatch.undo()
-    return np.max(np.abs(z_emu - z_ref)) / np.max(np.abs(z_ref))
-
-
 @pytest.mark.parametrize("name,B,N,H", [("tiny_gated", 2, 37, 2), ("small_gated", 2, 24, 2)])
-def test_gated_mlp_predictor_matches_oracle(monkeypatch, name, B, N, H):
+def test_gated_mlp_predictor_matches_oracle(name, B, N, H):
     """Gated-MLP variant (FC1 * GELU(FC2) up-projection, one GEMM over interleaved weights)
-    through the whole predictor, fp32 (SIMT) and bf16 (tcgen05) paths. The random-init gated
-    network amplifies activation rounding about twenty times more than the GELU one (in the
-    fp64 oracle, rounding only the LayerNorm outputs to bf16 moves the small gated frame by
-    ~5% against ~0.25%), so in bf16 the frame is held to twice that measured effect while the
-    energy keeps the stated 2e-2."""
+    through the whole predictor, fp32 (SIMT) and bf16 (tcgen05) paths, held to the same
+    bounds as the GELU network."""
     pc = synthetic.PRESETS[name]
     p = make_planner(name, max_horizon=2)
     z0, goal, s0, acts = _inputs(pc, B, N, H, seed=7)
@@ -154,12 +139,7 @@ def test_gated_mlp_predictor_matches_oracle(monkeypatch, name, B, N, H):
         if pc.precision == "fp32":
             assert zerr < TOL_FP32_REL and rel_err(en[b], e_ref) < TOL_FP32_REL
         else:
-            assert rel_err(en[b], e_ref) < TOL_BF16_ENERGY_REL
-            idx = np.arange(min(N, 4))
-            effect = _ln_rounding_effect(monkeypatch, name, pc, z0[b], s0[b], acts[b][idx], z_ref[idx])
-            zerr4 = np.max(np.abs(zp[b][idx] - z_ref[idx])) / np.max(np.abs(z_ref[idx]))
-            assert zerr4 < max(5e-2, 2 * effect), (zerr4, effect)
-            print(f"  LN-rounding effect {effect:.2e}")
+            assert rel_err(en[b], e_ref) < TOL_BF16_ENERGY_REL and zerr < 5e-2
         print(f"{name} b={b}: energy rel err {rel_err(en[b], e_ref):.2e}, z rel err {zerr:.2e}")
     p.close()
 

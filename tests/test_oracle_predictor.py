@@ -179,6 +179,19 @@ def test_gated_weights_in_canonical_order():
     assert np.array_equal(wb["l0.W_g"], predictor.round_to_bf16(synthetic.make_weights(cfg)["l0.W_g"]))
 
 
+@pytest.mark.parametrize("kind", ["gelu", "gated"])
+def test_synthetic_weight_recipe(kind):
+    """The input recipe: every matrix and bias N(0, 0.02); only the LayerNorm gains are
+    1 + N(0, 0.02) (the gate matrix W_g and bias b_g are ordinary weights, not gains)."""
+    cfg = dataclasses.replace(synthetic.SMALL, mlp_kind=kind)
+    w = synthetic.make_weights(cfg)
+    for name, v in w.items():
+        v = v.astype(np.float64)
+        gain = name.split(".")[-1] in ("ln1_g", "ln2_g", "lnf_g")
+        assert abs(v.mean() - (1.0 if gain else 0.0)) < 0.01, name
+        assert abs(v.std() - 0.02) < 0.005, name
+
+
 def _incremental_rollout(w, cfg, z0, s0, actions):
     """Independent KV-cached rollout: each layer attends over cached keys/values of earlier blocks."""
     n, H, _ = actions.shape
