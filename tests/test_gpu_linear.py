@@ -46,7 +46,7 @@ def test_linear_bf16_matches_matmul(planner, M, N, K, gelu):
 
 
 def test_gelu_epilogue_against_exact_erf(planner):
-    """GELU of the GEMM epilogue (erf by Abramowitz & Stegun 7.1.26) against the exact-erf
+    """GELU of the GEMM epilogue (erf by Abramowitz & Stegun 7.1.28) against the exact-erf
     GELU: with W = I the output is gelu(A) for bf16-representable A over [-8, 8]."""
     K = N = 64
     M = 2048
