@@ -38,8 +38,8 @@ from cem_search_transformer_gb300 import synthetic  # noqa: E402
 METRIC = "CEM plan-step latency (ms, 800x10) and candidate rollouts/sec, % of roofline"
 # DRAM bytes per launch of the four per-layer GEMMs (QKV, out-projection, MLP up, MLP down)
 # on the full-shape workload, from one ncu capture (profiles/gemm_attention_counters.md).
-GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (429.1e6 + 1216.1e6, 1270.7e6 + 786.4e6, 431.4e6 + 1633.1e6,
-                                   2658.9e6 + 828.3e6)
+GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (429e6 + 1220e6, 1271e6 + 793e6, 432e6 + 1644e6,
+                                   2683e6 + 834e6)
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -667,6 +667,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
       int stage = 0;
       uint32_t phase = 0;
       bool issued_any = false;
+      // A rows are read by the num_n CTA pairs that share a row block, at times that drift
+      // apart over a long K loop: keep them in L2 ahead of the streaming epilogue traffic
+      const uint64_t a_policy = l2_policy_evict_last();
       for (int t = cid; t < total; t += ncl) {
         const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n0 = (t % num_n) * BN + (int)rank * 128;
         bool ok = true;
@@ -678,7 +681,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
           const uint32_t sa = sbase + stage * C::STAGE_BYTES;
           const uint32_t lfull = map_to_rank(full_bar(stage), 0);
           if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
-          tma_load_2d_pair(sa, &tmA, kb * BKE, m0, lfull);
+          tma_load_2d_pair_hint(sa, &tmA, kb * BKE, m0, lfull, a_policy);
           tma_load_2d_pair(sa + C::A_BYTES, &tmB, kb * BKE, n0, lfull);
           issued_any = true;
           if (++stage == C::STAGES) stage = 0, phase ^= 1u;
