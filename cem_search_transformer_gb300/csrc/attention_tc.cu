@@ -63,6 +63,12 @@ __device__ __forceinline__ float ex2f(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// max of three (sm_100-family three-input max.f32)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
 
 }  // namespace
 
@@ -263,14 +269,14 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
           for (int c = 0; c < 64; ++c)
             if (c >= kv_left) s[c] = -INFINITY;
         }
-        // row max as a tree (8 independent chains, then combine)
+        // row max as a tree of three-input maxima (8 independent chains, then combine)
         float part[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          part[q] = fmaxf(fmaxf(fmaxf(s[8 * q], s[8 * q + 1]), fmaxf(s[8 * q + 2], s[8 * q + 3])),
-                          fmaxf(fmaxf(s[8 * q + 4], s[8 * q + 5]), fmaxf(s[8 * q + 6], s[8 * q + 7])));
-        const float cmax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                                 fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+          part[q] = fmax3(fmax3(s[8 * q], s[8 * q + 1], s[8 * q + 2]),
+                          fmax3(s[8 * q + 3], s[8 * q + 4], s[8 * q + 5]), fmaxf(s[8 * q + 6], s[8 * q + 7]));
+        const float cmax = fmax3(fmax3(part[0], part[1], part[2]), fmax3(part[3], part[4], part[5]),
+                                 fmaxf(part[6], part[7]));
         // The exponent reference m only moves when the row max grows by more than 8 (log2
         // units): until then P = 2^(s c - m c) stays <= 256, and since the same m scales the
         // numerator (O) and the denominator (l), the result is unchanged. Most chunks then
@@ -279,9 +285,11 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         const float mnew = bump ? fmaxf(m, cmax) : m;
         const float alpha = ex2f((m - mnew) * scale_log2);   // 1 when m is kept, 0 at j = 0
         const float ms = mnew * scale_log2;
-        // exponentiate and sum, packing P as bf16 pairs (key 2c in the low half of column c)
+        // exponentiate and sum, packing P as bf16 pairs (key 2c in the low half of column c);
+        // the exponent arguments and the row sum in packed f32x2 arithmetic
         uint32_t pk[32];
-        float rsp[8];
+        unsigned long long rsp[8];
+        const unsigned long long sc2 = f2_pack(scale_log2, scale_log2), nms2 = f2_pack(-ms, -ms);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           float e[8];
@@ -291,9 +299,14 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
             for (int t = 0; t < 8; ++t) e[t] = 0.f;
           } else {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) e[t] = ex2f(fmaf(s[8 * cc + t], scale_log2, -ms));
+            for (int t = 0; t < 4; ++t) {
+              const float2 a = f2_unpack(f2_fma(f2_pack(s[8 * cc + 2 * t], s[8 * cc + 2 * t + 1]), sc2, nms2));
+              e[2 * t] = ex2f(a.x);
+              e[2 * t + 1] = ex2f(a.y);
+            }
           }
-          rsp[cc] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+          rsp[cc] = f2_add(f2_add(f2_pack(e[0], e[1]), f2_pack(e[2], e[3])),
+                           f2_add(f2_pack(e[4], e[5]), f2_pack(e[6], e[7])));
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             __nv_bfloat162 pp = __floats2bfloat162_rn(e[2 * t], e[2 * t + 1]);
@@ -302,7 +315,9 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         }
         // S of this chunk is in registers: P takes its first 32 columns
         tmem_st32(tSg + lane_off, pk);
-        const float rs = ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
+        const float2 rs2 = f2_unpack(f2_add(f2_add(f2_add(rsp[0], rsp[1]), f2_add(rsp[2], rsp[3])),
+                                            f2_add(f2_add(rsp[4], rsp[5]), f2_add(rsp[6], rsp[7]))));
+        const float rs = rs2.x + rs2.y;
         l = l * alpha + rs;
         m = mnew;
         // P V of the previous chunk must be complete before O is rescaled and P handed over
