@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
           mma_bf16_ts(tO(ii), tS(gg) + 8u * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), idO,
                       (j > 0) || (kk > 0));
         mma_commit(o_full);
-        mma_commit(kv_empty(gg % KV_STAGES));
-        if (j == nch - 1) mma_commit(q_empty(ii & 1));
+        // the K/V stage and (after an item's last chunk) the Q buffer are released by softmax
+        // warp 2 once it has seen this P V complete, which keeps those commits off this thread
         // tensor-core operations of this thread run in issue order, so the scores of chunk
         // gg + 2 overwrite this S / P buffer only after the P V above has read it
         if (gg + 2 < total) {
@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
             ok = false;
             break;
           }
+          if (j > 0 && warp == 2 && lane == 0) mbar_arrive(kv_empty((g - 1) % KV_STAGES));
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(p_full);
@@ -320,13 +321,15 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         const float rs = rs2.x + rs2.y;
         l = l * alpha + rs;
         m = mnew;
-        // P V of the previous chunk must be complete before O is rescaled and P handed over
+        // P V of the previous chunk must be complete before O is rescaled and P handed over;
+        // its K/V stage is then free for the producer
         if (j > 0) {
           if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          if (warp == 2 && lane == 0) mbar_arrive(kv_empty((g - 1) % KV_STAGES));
         }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
           uint32_t ov[32], ow[32];
@@ -351,6 +354,10 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
       // end of the item: wait for its last P V, normalise O, store, hand the O buffer back
       if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) break;
       tc_fence_after();
+      if (warp == 2 && lane == 0) {
+        mbar_arrive(kv_empty((g - 1) % KV_STAGES));   // the item's last K/V stage
+        mbar_arrive(q_empty(i & 1));                   // and its Q tile
+      }
       if (active) {
         const float inv = 1.f / l;
         const int t = qt * AQ + row;
