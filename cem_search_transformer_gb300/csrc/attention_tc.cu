@@ -17,12 +17,16 @@
 //                 O += P V    (M 128, N 64, K 64; P read from TMEM, V read MN-major
 //                              straight from its TMA tile)
 //               Chunk g's scores go to S buffer g % 2; the scores of chunk g + 2 are issued
-//               right after P V of chunk g, which has consumed that buffer;
+//               right after P V of chunk g, which has consumed that buffer. This thread
+//               bounds the kernel (it issues eight short MMAs per 64 keys), so it does
+//               nothing else: it commits only S and P V completion;
 //   warps 2-5   softmax, one query row per thread: read S from TMEM, online max / sum,
 //               write P (bf16, two per column) over the first 32 columns of the same S
 //               buffer, rescale O in TMEM, and at the end of an item normalise O and store it.
 //               The exponentials of chunk g overlap P V of chunk g - 1: only the O rescale
-//               (rare, see below) and the hand-over of P wait for it.
+//               (rare, see below) and the hand-over of P wait for it. Warp 2, having seen a
+//               chunk's P V complete, also hands its K/V stage (and an item's Q tile after
+//               its last chunk) back to the producer.
 // TMEM: S / P buffers in columns [0, 64) and [192, 256), O of even items in [64, 128), of
 // odd items in [128, 192), so one item's output read-out overlaps the next item's MMAs.
 // In a partial last tile the rows of inactive warps keep stale words in P; their O rows

@@ -7,18 +7,22 @@
 //   - warp 0: TMA producer (128B-swizzled 128x64 A and BNx64 W boxes into a STAGES-deep ring);
 //   - warp 1: TMEM allocator and single-thread tcgen05.mma issuer (M=128, N=BN, K=16 per
 //     instruction), committing to "smem empty" barriers and to a per-accumulator "full" barrier;
-//   - warps 2..: epilogue, EW warps in all (8, or 16 for the GELU layer whose erf is the
-//     expensive part), EW/4 warps per TMEM lane quarter, each taking a 4/EW share of the
-//     tile's columns. A warp reads 32 rows x 32 columns with tcgen05.ld 32x32b.x32 (thread = row),
-//     transposes them through a swizzled 4 KB shared-memory buffer so that each global
-//     access covers contiguous columns of a row, and applies bias / GELU / residual /
-//     position / L1 energy (see common.cuh) four columns at a time. The next chunk's TMEM
-//     load is in flight while the current chunk is processed.
+//   - warps 2..: epilogue, EW warps in all (8, or 16 for the GELU and gated layers whose
+//     erf is the expensive part), EW/4 warps per TMEM lane quarter, each taking a 4/EW
+//     share of the tile's columns. A warp reads 32 rows x 32 columns with tcgen05.ld
+//     32x32b.x32 (thread = row). The GELU and gated epilogues apply bias and activation in
+//     that layout and stage only bf16 results; the others transpose fp32 accumulators
+//     through a swizzled 4 KB shared-memory buffer so that each global access covers
+//     contiguous columns of a row, and apply bias / residual / position / L1 energy (see
+//     common.cuh) four columns at a time. The next chunk's TMEM load is in flight while the
+//     current chunk is processed.
 //   - two TMEM accumulators (2 x BN columns) so the epilogue of tile i overlaps the MMAs of
 //     tile i+1;
 //   - QKV, the MLP up-projection and the residual projections run on CTA pairs
-//     (k_gemm_tc2: 256 x 256 tiles with tcgen05.mma.cta_group::2), the projections to and
-//     from the embedding space and small or ragged shapes on single CTAs (k_gemm_tc).
+//     (k_gemm_tc2: 256 x 256 tiles with tcgen05.mma.cta_group::2, A loaded with an L2
+//     evict_last policy so that the pairs sharing a row block find it in L2), the
+//     projections to and from the embedding space and small or ragged shapes on single
+//     CTAs (k_gemm_tc).
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the kernel records an
 // error flag, stops issuing work, waits (bounded) for its own copies and MMAs, frees TMEM
 // and returns.
