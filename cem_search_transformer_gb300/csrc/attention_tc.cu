@@ -173,31 +173,39 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
       constexpr uint32_t idS = idesc_bf16(AQ, AK, false);
       constexpr uint32_t idO = idesc_bf16(AQ, AHD, true);
       const int total = my_items * nch;
-      auto issue_s = [&](int gg) {
-        // the chunk gg belongs to item gg / nch, whose Q sits in buffer (gg / nch) & 1
-        const int ii = gg / nch;
-        const uint64_t qdesc = desc_sw128(sb + OFF_Q + (ii & 1) * Q_BYTES);
+      // (item, chunk within the item) of the chunk being multiplied by V and of the next
+      // chunk whose scores are issued, advanced by counting (no divisions on this thread,
+      // which bounds the kernel)
+      auto advance = [&](int& it, int& jj) {
+        if (++jj == nch) {
+          jj = 0;
+          ++it;
+        }
+      };
+      auto issue_s = [&](int gg, int it) {   // chunk gg of item it, whose Q sits in buffer it & 1
+        const uint64_t qdesc = desc_sw128(sb + OFF_Q + (it & 1) * Q_BYTES);
         const uint64_t kdesc = desc_sw128(sb + OFF_K + (gg % KV_STAGES) * KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < AHD / 16; ++kk)
           mma_bf16_ss(tS(gg), qdesc + 2 * kk, kdesc + 2 * kk, idS, kk > 0);
         mma_commit(s_full(gg & 1));
       };
-      auto ready_s = [&](int gg) {   // operands of S for chunk gg are in shared memory
-        const int ii = gg / nch;
-        if (gg % nch == 0 && !mbar_wait(q_full(ii & 1), (ii >> 1) & 1, abort_flag, err_flag)) return false;
+      auto ready_s = [&](int gg, int it, int jj) {   // operands of S for chunk gg in shared memory
+        if (jj == 0 && !mbar_wait(q_full(it & 1), (it >> 1) & 1, abort_flag, err_flag)) return false;
         return mbar_wait(kv_full(gg % KV_STAGES), (gg / KV_STAGES) & 1, abort_flag, err_flag);
       };
       bool ok = true;
+      int si = 0, sj = 0;   // next chunk whose scores are issued
       for (int gg = 0; gg < 2 && gg < total && ok; ++gg) {
-        ok = ready_s(gg);
+        ok = ready_s(gg, si, sj);
         if (ok) {
           tc_fence_after();
-          issue_s(gg);
+          issue_s(gg, si);
+          advance(si, sj);
         }
       }
-      for (int gg = 0; gg < total && ok; ++gg) {
-        const int ii = gg / nch, j = gg % nch;
+      int ii = 0, j = 0;
+      for (int gg = 0; gg < total && ok; ++gg, advance(ii, j)) {
         if (!mbar_wait(p_full, gg & 1, abort_flag, err_flag)) break;
         // the O buffer of this item was last read out for item ii - 2
         if (j == 0 && ii >= 2 && !mbar_wait(o_free(ii & 1), ((ii >> 1) - 1) & 1, abort_flag, err_flag))
@@ -214,9 +222,10 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         // tensor-core operations of this thread run in issue order, so the scores of chunk
         // gg + 2 overwrite this S / P buffer only after the P V above has read it
         if (gg + 2 < total) {
-          if (!ready_s(gg + 2)) break;
+          if (!ready_s(gg + 2, si, sj)) break;
           tc_fence_after();
-          issue_s(gg + 2);
+          issue_s(gg + 2, si);
+          advance(si, sj);
         }
       }
       mma_commit(teardown);
