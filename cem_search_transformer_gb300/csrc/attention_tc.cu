@@ -28,7 +28,10 @@
 //               chunk's P V complete, also hands its K/V stage (and an item's Q tile after
 //               its last chunk) back to the producer.
 // TMEM: S / P buffers in columns [0, 64) and [192, 256), O of even items in [64, 128), of
-// odd items in [128, 192), so one item's output read-out overlaps the next item's MMAs.
+// odd items in [128, 192). An item's output is read out (normalised, stored) right after
+// the next item's first P hand-over, so the read-out overlaps that chunk's P V instead of
+// delaying it; the P hand-over and P V completion barriers alternate by chunk parity, which
+// keeps every warp within one phase of each barrier while it postpones that wait.
 // In a partial last tile the rows of inactive warps keep stale words in P; their O rows
 // are computed from them but never read. Keys past Lk are masked to
 // -inf (their P is 0; the K/V rows loaded there are finite: cache rows are zero-initialised
@@ -55,9 +58,9 @@ constexpr int OFF_Q = 0;                  // two Q buffers
 constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
 constexpr int OFF_V = OFF_K + KV_STAGES * KV_BYTES;
 constexpr int OFF_BAR = OFF_V + KV_STAGES * KV_BYTES;
-// q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full, o_full, o_free[2],
-// teardown
-constexpr int NUM_BARS = 4 + 2 * KV_STAGES + 2 + 2 + 2 + 1;
+// q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2],
+// o_free[2], teardown
+constexpr int NUM_BARS = 4 + 2 * KV_STAGES + 2 + 2 + 2 + 2 + 1;
 constexpr int A_SMEM = OFF_BAR + NUM_BARS * 8 + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr int CTAS_PER_SM = 2;
@@ -90,9 +93,12 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
   auto kv_empty = [&](int s) { return bar + 8u * (4 + KV_STAGES + s); };
   const uint32_t s_full0 = bar + 8u * (4 + 2 * KV_STAGES);
   auto s_full = [&](int b) { return s_full0 + 8u * b; };
-  const uint32_t p_full = s_full0 + 16, o_full = s_full0 + 24;
-  auto o_free = [&](int b) { return s_full0 + 32 + 8u * b; };
-  const uint32_t teardown = s_full0 + 48;
+  // chunk g's P hand-over and P V completion use barrier g % 2 of each pair: a warp is then
+  // never more than one phase ahead on either, so it may postpone a wait on o_full
+  auto p_full = [&](int b) { return s_full0 + 16 + 8u * b; };
+  auto o_full = [&](int b) { return s_full0 + 32 + 8u * b; };
+  auto o_free = [&](int b) { return s_full0 + 48 + 8u * b; };
+  const uint32_t teardown = s_full0 + 64;
   uint32_t* tmem_slot = (uint32_t*)(smem + OFF_BAR + NUM_BARS * 8);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
@@ -120,8 +126,10 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
     }
     mbar_init(s_full(0), 1);
     mbar_init(s_full(1), 1);
-    mbar_init(p_full, 4);
-    mbar_init(o_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(p_full(b), 4);
+      mbar_init(o_full(b), 1);
+    }
     mbar_init(teardown, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -206,7 +214,7 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
       }
       int ii = 0, j = 0;
       for (int gg = 0; gg < total && ok; ++gg, advance(ii, j)) {
-        if (!mbar_wait(p_full, gg & 1, abort_flag, err_flag)) break;
+        if (!mbar_wait(p_full(gg & 1), (gg >> 1) & 1, abort_flag, err_flag)) break;
         // the O buffer of this item was last read out for item ii - 2
         if (j == 0 && ii >= 2 && !mbar_wait(o_free(ii & 1), ((ii >> 1) - 1) & 1, abort_flag, err_flag))
           break;
@@ -216,7 +224,7 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         for (int kk = 0; kk < AK / 16; ++kk)  // 16 keys: 8 TMEM columns of P, 16 rows x 128 B of V
           mma_bf16_ts(tO(ii), tS(gg) + 8u * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), idO,
                       (j > 0) || (kk > 0));
-        mma_commit(o_full);
+        mma_commit(o_full(gg & 1));
         // the K/V stage and (after an item's last chunk) the Q buffer are released by softmax
         // warp 2 once it has seen this P V complete, which keeps those commits off this thread
         // tensor-core operations of this thread run in issue order, so the scores of chunk
@@ -238,6 +246,54 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto po_wait = [&](int gc) {   // P V of chunk gc complete
+      return mbar_wait(o_full(gc & 1), (gc >> 1) & 1, abort_flag, err_flag);
+    };
+    // An item's output is read out after the next item's first P hand-over, so that the
+    // read-out overlaps that chunk's P V instead of delaying it.
+    struct Pending {
+      int i, qt, h, cand, glast;
+      bool active;
+      float l;
+    } pend = {-1, 0, 0, 0, 0, false, 0.f};
+    auto finish_item = [&](const Pending& it) {
+      if (!po_wait(it.glast)) return false;
+      tc_fence_after();
+      if (warp == 2 && lane == 0) {
+        mbar_arrive(kv_empty(it.glast % KV_STAGES));   // the item's last K/V stage
+        mbar_arrive(q_empty(it.i & 1));                 // and its Q tile
+      }
+      if (it.active) {
+        const float inv = 1.f / it.l;
+        const int t = it.qt * AQ + row;
+        bf16* orow = o + ((long long)it.cand * T + t) * d + it.h * AHD;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t ov[32];
+          tmem_ld32_async(tO(it.i) + lane_off + 32 * hf, ov);
+          tmem_wait(ov);
+          if (t < T) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint4 u;
+              __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+              __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+              __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+              __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+              u.x = *reinterpret_cast<uint32_t*>(&p0);
+              u.y = *reinterpret_cast<uint32_t*>(&p1);
+              u.z = *reinterpret_cast<uint32_t*>(&p2);
+              u.w = *reinterpret_cast<uint32_t*>(&p3);
+              *reinterpret_cast<uint4*>(orow + 32 * hf + c) = u;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free(it.i & 1));
+      return true;
+    };
     bool ok = true;
     int g = 0;
     for (int i = 0; i < my_items && ok; ++i) {
@@ -256,14 +312,23 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         }
         tc_fence_after();
         if (!active) {
-          if (j > 0 && !mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
-            ok = false;
-            break;
+          if (j > 0) {
+            if (!po_wait(g - 1)) {
+              ok = false;
+              break;
+            }
+            if (warp == 2 && lane == 0) mbar_arrive(kv_empty((g - 1) % KV_STAGES));
           }
-          if (j > 0 && warp == 2 && lane == 0) mbar_arrive(kv_empty((g - 1) % KV_STAGES));
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(p_full);
+          if (lane == 0) mbar_arrive(p_full(g & 1));
+          if (j == 0 && pend.i >= 0) {
+            if (!finish_item(pend)) {
+              ok = false;
+              break;
+            }
+            pend.i = -1;
+          }
           continue;
         }
         uint32_t sa[32], sc[32];
@@ -337,7 +402,7 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         // P V of the previous chunk must be complete before O is rescaled and P handed over;
         // its K/V stage is then free for the producer
         if (j > 0) {
-          if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) {
+          if (!po_wait(g - 1)) {
             ok = false;
             break;
           }
@@ -361,46 +426,19 @@ __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
-      }
-      if (!ok) break;
-      // end of the item: wait for its last P V, normalise O, store, hand the O buffer back
-      if (!mbar_wait(o_full, (g - 1) & 1, abort_flag, err_flag)) break;
-      tc_fence_after();
-      if (warp == 2 && lane == 0) {
-        mbar_arrive(kv_empty((g - 1) % KV_STAGES));   // the item's last K/V stage
-        mbar_arrive(q_empty(i & 1));                   // and its Q tile
-      }
-      if (active) {
-        const float inv = 1.f / l;
-        const int t = qt * AQ + row;
-        bf16* orow = o + ((long long)cand * T + t) * d + h * AHD;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t ov[32];
-          tmem_ld32_async(tOi + lane_off + 32 * hf, ov);
-          tmem_wait(ov);
-          if (t < T) {
-#pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint4 u;
-              __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-              __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-              __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-              __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-              u.x = *reinterpret_cast<uint32_t*>(&p0);
-              u.y = *reinterpret_cast<uint32_t*>(&p1);
-              u.z = *reinterpret_cast<uint32_t*>(&p2);
-              u.w = *reinterpret_cast<uint32_t*>(&p3);
-              *reinterpret_cast<uint4*>(orow + 32 * hf + c) = u;
-            }
+        if (lane == 0) mbar_arrive(p_full(g & 1));
+        if (j == 0 && pend.i >= 0) {
+          if (!finish_item(pend)) {
+            ok = false;
+            break;
           }
+          pend.i = -1;
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free(i & 1));
+      if (!ok) break;
+      pend = Pending{i, qt, h, cand, g - 1, active, l};
     }
+    if (ok && pend.i >= 0) finish_item(pend);
   }
   tc_fence_before();
   __syncthreads();
