@@ -83,6 +83,35 @@ def fp8_flop_split(pc, H):
     return float(f8), float(f16)
 
 
+def attention_flops(pc, H):
+    """Attention FLOPs per candidate rollout: per frame k, every layer and head takes T queries
+    over the (k + 1) T cached keys, Q K^T and P V at 2 FLOPs per multiply-add each."""
+    T, d, L = pc.tokens, pc.width, pc.layers
+    return float(sum(L * 4 * T * (k + 1) * T * d for k in range(H)))
+
+
+def step_roofline(pc, H, rollouts, gemm_tflop, step_ms, peaks):
+    """The whole plan step against the tensor-core roofline: executed GEMM FLOPs (measured
+    count if available) plus attention FLOPs, at the measured burst and sustained bf16 rates
+    and at the nominal 2.25 PFLOP/s dense bf16 of a GB300 (e4m3 GEMMs count at twice the
+    bf16 rate). The operand bytes (0.61 GB of weights per pass) are far below the FLOP time."""
+    f8, f16 = fp8_flop_split(pc, H)
+    if pc.precision != "fp8":
+        f8, f16 = 0.0, f8 + f16
+    gemm = f8 + f16
+    scale = (gemm_tflop * 1e12 / rollouts) / gemm if gemm_tflop else 1.0
+    f8, f16 = f8 * scale * rollouts, (f16 * scale + attention_flops(pc, H)) * rollouts
+    out = {"bound": "tensor", "tflop_per_step": (f8 + f16) / 1e12}
+    for key, tf in (("measured_burst", peaks.get("bf16_tflops", PEAK_FALLBACK["bf16_tflops"])),
+                    ("measured_sustained", peaks.get("bf16_tflops_sustained",
+                                                     PEAK_FALLBACK["bf16_tflops_sustained"])),
+                    ("nominal_dense", 2250.0)):
+        t_ms = (f8 / (2 * tf) + f16 / tf) / 1e12 * 1e3
+        out[f"ms_at_{key}"] = t_ms
+        out[f"frac_of_{key}"] = t_ms / step_ms
+    return out
+
+
 def workload_desc(wl):
     pc = wl.predictor
     return (f"{wl.predictor.name} CEM: {pc.layers}x{pc.width} predictor, heads {pc.heads}, "
@@ -331,6 +360,8 @@ def run_ours(args, wl):
                          "traffic_unit": "DRAM bytes per launch (mean of the four per-layer GEMMs)",
                          "gemm_share_of_step": (gemm_ms / prof_steps) / step_ms if gemm_launches else None,
                          "gemm_tflop_per_step": step_flops / 1e12 if step_flops else None},
+            "step_roofline": step_roofline(pc, H, N * R * B, step_flops / 1e12 if step_flops else None,
+                                           step_ms, peaks),
             "e2e": {"value": rollouts / (e2e_ms * 1e-3), "unit": "candidate rollouts/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,

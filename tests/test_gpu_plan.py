@@ -111,6 +111,39 @@ def test_full_shape_plan_teacher_forced():
     p.close()
 
 
+def test_multistep_full_shape_plan_teacher_forced():
+    """The multi-step workload (full-shape predictor, horizon 3: blocks z0, z1, z2 fed, z3
+    scored; N=800, K=80, R=10) in the launch configuration the benchmark times, with one
+    KV-cache slot per layer reused across the three frames. Every round is checked against
+    the oracle (sampler over all three steps, elites, refit); sampled energies come from the
+    oracle's three-frame rollout (a full recompute of the growing sequence, no cache), one of
+    them the final round's winner."""
+    wl = synthetic.WORKLOADS["multistep"]
+    pc, H = wl.predictor, wl.horizon
+    p = make_planner("full", max_horizon=H)
+    z0, goal, s0 = synthetic.make_problems(pc, 1)
+    mu0, sg0 = synthetic.make_gaussian(pc, 1, H)
+    out, tr = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    p.close()
+    for r in range(wl.rounds):
+        a_ref = philox.sample_actions(tr["mu"][r, 0], tr["sigma"][r, 0],
+                                      philox.sample_eps(wl.seed, 0, r, wl.N, H, 7))
+        assert np.max(np.abs(tr["actions"][r, 0] - a_ref)) < TOL_EPS
+        el = cem.select_elites(tr["energy"][r, 0], wl.K)
+        assert np.array_equal(el, tr["elites"][r, 0])
+        m_ref, s_ref = cem.refit(tr["actions"][r, 0][el])
+        assert np.max(np.abs(tr["mu"][r + 1, 0] - m_ref)) < TOL_REFIT
+        assert np.max(np.abs(tr["sigma"][r + 1, 0] - s_ref)) < TOL_REFIT
+    assert tr["winner"][0] == tr["elites"][-1, 0][0]
+    assert np.array_equal(out[0], tr["actions"][-1, 0][tr["winner"][0], 0])
+    # two sampled rollouts in one oracle call: round 0's candidate 611, the last round's winner
+    picks = ((0, 611), (wl.rounds - 1, int(tr["winner"][0])))
+    acts = np.stack([tr["actions"][r, 0][n] for r, n in picks]).astype(np.float64)
+    z = predictor.rollout(oracle_weights_for("full"), pc, z0[0], s0[0], acts)[-1]
+    e_gpu = np.array([tr["energy"][r, 0][n] for r, n in picks])
+    assert rel_err(e_gpu, predictor.energy_l1(z, goal[0])) < TOL_BF16_ENERGY_REL
+
+
 def test_sweep_batched_full_shape_teacher_forced():
     """A throughput-sweep cell at the full shape: B = 4 problems of N = 400 candidates share
     one candidate axis of 1600 rollouts, cut into chunks of 1024, so a chunk boundary falls
