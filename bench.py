@@ -25,6 +25,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -126,10 +127,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir: str = ""):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
@@ -270,7 +271,7 @@ def run_ours(args, wl):
     barrier()
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clocks_dir) as clk:
         ev0.record(stream)
         for _ in range(args.steps):
             planner.plan(dz0, ds0, dgoal, dmu, dsg, B, H, N, K, R, wl.seed, out, stream=stream)
@@ -405,7 +406,7 @@ def run_closed_loop(args, wl):
         run()
     planner.sync_check(stream)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(0) as clk:
+    with ClockSampler(0, args.clocks_dir) as clk:
         ev0.record(stream)
         for _ in range(args.steps):
             run()
@@ -447,6 +448,8 @@ def main():
                          "its CUDA graph (for the graph-vs-stream comparison)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default="",
+                    help="directory for the raw nvidia-smi samples (default: the temp directory)")
     args = ap.parse_args()
     wl = synthetic.WORKLOADS[args.workload]
     if args.candidates:
