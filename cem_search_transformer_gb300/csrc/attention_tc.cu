@@ -455,16 +455,17 @@ cudaError_t attention_tc_bf16(const bf16* q, const bf16* kv, bf16* o, int ncand,
   if (ncand <= 0) return cudaSuccess;
   const int nq = (T + AQ - 1) / AQ;
   if (d != heads * AHD || d % 8) return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  static int num_sms = 0;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_attention_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         A_SMEM);
-    if (e != cudaSuccess) return e;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    attr_done = true;
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = set_max_dynamic_smem((const void*)k_attention_tc, A_SMEM, attr_done);
+  if (e != cudaSuccess) return e;
+  static std::atomic<int> sms_of_device[64];   // SM count per device ordinal, 0 = not read yet
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  int num_sms = (dev >= 0 && dev < 64) ? sms_of_device[dev].load(std::memory_order_relaxed) : 0;
+  if (num_sms <= 0) {
+    if ((e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    if (dev >= 0 && dev < 64) sms_of_device[dev].store(num_sms, std::memory_order_relaxed);
   }
   CUtensorMap mq, mkv;
   if (!make_map(&mq, q, ncand * T, d, AQ, AHD) ||

@@ -5,9 +5,26 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace jepa {
 
 typedef __nv_bfloat16 bf16;
+
+// cudaFuncSetAttribute acts on the current device only. Each kernel that needs more than
+// 48 KB of dynamic shared memory keeps a mask of the devices (ordinals 0..63) it has been
+// configured on; a device outside the mask range is configured on every call.
+inline cudaError_t set_max_dynamic_smem(const void* func, int bytes,
+                                        std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Row remap used by epilogues and row-gathering kernels:
 //   r -> (r / rpg) * gstride + goff + (r % rpg)

@@ -782,13 +782,9 @@ template <int BN, int MODE, int OP>
 static cudaError_t launch_tc(const void* A, const void* W, int M, int N, int K, const Epilogue& epi,
                              int* err_flag, int num_sms, cudaStream_t s) {
   using C = Cfg<BN, MODE>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, MODE, OP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = set_max_dynamic_smem((const void*)k_gemm_tc<BN, MODE, OP>, C::SMEM, attr_done);
+  if (e != cudaSuccess) return e;
   CUtensorMap ma, mb;
   if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, BN))
     return cudaErrorInvalidValue;
@@ -824,13 +820,9 @@ template <int MODE, int OP>
 static cudaError_t launch_tc2(const void* A, const void* W, int M, int N, int K, const Epilogue& epi,
                               int* err_flag, int num_sms, cudaStream_t s) {
   using C = Cfg2<MODE>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc2<MODE, OP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = set_max_dynamic_smem((const void*)k_gemm_tc2<MODE, OP>, C::SMEM, attr_done);
+  if (e != cudaSuccess) return e;
   CUtensorMap ma, mb;
   if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, 128))
     return cudaErrorInvalidValue;
