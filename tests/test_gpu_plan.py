@@ -74,6 +74,38 @@ def test_tiny_fp32_plan_matches_oracle():
     p.close()
 
 
+def test_tiny_fp32_plan_end_to_end_reachable_goal():
+    """A whole plan against the oracle's, without teacher forcing. With the synthetic
+    recipe's independent goal the energies of this random-init predictor's candidates differ
+    by ~1e-5 relative, below the fp32 tolerance, so the tolerance does not decide the elites.
+    Here the goal is the oracle's own predicted frame for a hidden action, which spreads the
+    energies by ~20 %: every round's K-th / (K+1)-th gap and the final winner's lead then
+    exceed the tolerance (asserted on the oracle's plan), and the GPU must pick the oracle's
+    elites in every round, refit to its mean and std, and return its action."""
+    wl = synthetic.WORKLOADS["tiny"]
+    pc = wl.predictor
+    z0, _, s0 = synthetic.make_problems(pc, 1)
+    mu0, sg0 = synthetic.make_gaussian(pc, 1, wl.horizon)
+    astar = synthetic.make_actions(pc, 1, 1, wl.horizon, seed=99)[0].astype(np.float64)
+    goal = predictor.rollout(oracle_weights_for("tiny"), pc, z0[0], s0[0], astar)[-1][0]
+    goal = goal[None].astype(np.float32)
+    ref = cem.plan(synthetic.make_weights(pc), pc, z0[0], s0[0], goal[0], mu0[0], sg0[0], wl.N,
+                   wl.K, wl.rounds, wl.seed)
+    for e in ref["energy"]:
+        assert energy_gap_allows(e, wl.K, TOL_FP32_REL)
+    assert energy_gap_allows(ref["energy"][-1], 1, TOL_FP32_REL)   # the winner is unique
+    p = make_planner("tiny", max_horizon=wl.horizon)
+    out, tr = _plan(p, pc, wl, z0, goal, s0, mu0, sg0)
+    p.close()
+    for r in range(wl.rounds):
+        assert set(tr["elites"][r, 0]) == set(ref["elites"][r])
+        assert rel_err(tr["energy"][r, 0], ref["energy"][r]) < TOL_FP32_REL
+        assert np.max(np.abs(tr["mu"][r + 1, 0] - ref["mu"][r + 1])) < 1e-5
+        assert np.max(np.abs(tr["sigma"][r + 1, 0] - ref["sigma"][r + 1])) < 1e-5
+    assert tr["winner"][0] == ref["winner"]
+    assert np.max(np.abs(out[0] - ref["action"])) < 1e-5
+
+
 def test_small_bf16_plan_teacher_forced():
     wl = synthetic.WORKLOADS["small"]
     pc = wl.predictor
