@@ -2,8 +2,8 @@
 // (SIMT) GEMM and attention used by the fp32 precision mode.
 //
 // Method: "Real-time inference for JEPA world-model architectures with Ray", section
-// "Where the sixteen seconds actually goes" (draw candidates from a Gaussian, score
-// against the goal, keep the best K, re-centre the Gaussian).
+// "Where the sixteen seconds actually goes" (sample from a Gaussian, measure each
+// sample's distance to the goal, refit the Gaussian to the K closest).
 #include "common.cuh"
 #include "tc_common.cuh"
 

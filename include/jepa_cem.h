@@ -3,11 +3,11 @@
  * JEPA world-model predictor.
  *
  * What it computes follows "Real-time inference for JEPA world-model architectures
- * with Ray", section "Where the sixteen seconds actually goes": one planning step
- * draws N candidate action sequences from a Gaussian, pushes each through the
- * predictor, scores the prediction against the goal embedding, keeps the best K,
- * re-centres the Gaussian on them, repeats for R rounds and returns only the first
- * action of the winning sequence. Section "Measured on 8x A100" adds that the
+ * with Ray", section "Where the sixteen seconds actually goes": in each of R rounds a
+ * planning step samples N action sequences from a Gaussian, predicts with the world
+ * model where each one leads, measures how far each predicted embedding lies from the
+ * goal embedding and refits the Gaussian to the K closest; the caller receives only
+ * the first action of the closest sequence of the last round. Section "Measured on 8x A100" adds that the
  * predictor is frame-causal (so a KV cache across rollout steps is exact), that it
  * runs in bf16 with flash attention, and that the same seed gives the same plan
  * however the candidates are batched.
@@ -122,8 +122,8 @@ size_t jepa_weight_blob_bytes(const jepa_config* cfg);
  * previously loaded weights (if any) stay in place. */
 jepa_status jepa_load_weights(jepa_ctx* ctx, const void* host_blob, size_t bytes);
 
-/* Candidate sampler (planning page: "draws 800 candidate action sequences from a
- * Gaussian centered on its current best guess").
+/* Candidate sampler (the planning page, "Where the sixteen seconds actually goes": each
+ * round's candidate action sequences are drawn from a Gaussian around the current guess).
  *   mu, sigma [B,H,A] dev; actions [B,N,H,A] dev (output).
  * eps[b,n,h,j] comes from Philox4x32-10 with key (seed lo, seed hi) and counter
  * (n, b, round*Q + q, 0), Q = ceil(H*A/4), q = (h*A+j)/4, word (h*A+j)%4, turned into
@@ -138,8 +138,9 @@ jepa_status jepa_sample_actions(jepa_ctx* ctx, const float* mu, const float* sig
 jepa_status jepa_philox4x32_10(jepa_ctx* ctx, const uint32_t* counters, uint64_t seed, int n,
                                uint32_t* out, void* stream);
 
-/* Predictor rollout and L1 energy (the "push every one through the predictor, score
- * the results against the goal embedding" step; frame-causal with a KV cache).
+/* Predictor rollout and L1 energy (the step of the same section that rolls every candidate
+ * through the predictor and scores the outcome against the goal embedding; frame-causal
+ * with a KV cache).
  *   z_ctx [B,P,E] dev   encoded context frame of each problem
  *   state0 [B,S] dev    state of each problem (s_k = s_{k-1} + a_{k-1})
  *   actions [B,N,H,A] dev
@@ -151,8 +152,9 @@ jepa_status jepa_predictor_forward(jepa_ctx* ctx, const float* z_ctx, const floa
                                    const float* actions, int B, int N, int H, const float* goal,
                                    float* z_pred, float* energy, void* stream);
 
-/* Elite selection and Gaussian refit ("keeps the best 80, and re-centers the Gaussian on
- * them"): per problem, the K lowest energies ordered by (energy, index), NaN last; then
+/* Elite selection and Gaussian refit (the same section: the best K candidates are kept and
+ * the Gaussian is moved onto them): per problem, the K lowest energies ordered by
+ * (energy, index), NaN last; then
  * mu' = elite mean and sigma' = elite population std per (h, j).
  *   energy [B,N] dev; actions [B,N,H,A] dev; mu_out, sigma_out [B,H,A] dev (outputs);
  *   elites_out [B,K] int32 dev or NULL. 1 <= K <= N <= 8192. */

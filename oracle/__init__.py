@@ -9,10 +9,11 @@ CUDA path; both take their inputs from ``cem_search_transformer_gb300.synthetic`
 The oracle is plain numpy in float64 (library matmul/erf as primitives, no
 blocking or fusion), written step by step from "Real-time inference for JEPA
 world-model architectures with Ray" (section "Where the sixteen seconds actually
-goes"): draw candidates from a Gaussian, push each through the predictor, score
-against the goal embedding, keep the best K, re-centre the Gaussian, repeat for
-R rounds, return the first action of the winner. Where the page is silent the
-module docstrings state the reading taken.
+goes"): sample action sequences from a Gaussian, predict where each leads,
+measure the distance of each prediction to the goal embedding, refit the Gaussian
+to the K closest, and after R rounds hand back the first action of the closest
+final-round sequence. Where the page is silent the module docstrings state the
+reading taken.
 
 Modules:
   philox     counter-based Philox4x32-10 + Box-Muller candidate sampler

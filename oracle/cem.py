@@ -2,10 +2,10 @@
 
 Test infrastructure (see the package docstring). Follows "Real-time inference for
 JEPA world-model architectures with Ray", section "Where the sixteen seconds
-actually goes": each round draws N candidate action sequences from a Gaussian
-centred on the current guess, scores every one, keeps the best K and re-centres
-the Gaussian on them; after R rounds only the first action of the winning
-sequence is executed.
+actually goes": in every round N action sequences are sampled from the current
+Gaussian and given an energy, and the Gaussian is refitted to the K of lowest
+energy; after R rounds the first action of the final round's lowest-energy
+sequence is the output.
 
 Readings taken where the page is silent:
   * "best" = lowest energy; ties go to the lower candidate index; NaN ranks last;
