@@ -5,7 +5,7 @@
 // section "Where the sixteen seconds actually goes") is captured once per
 // (B, H, N, K, R) as a single CUDA graph: rounds follow each other on the device with
 // mu/sigma kept in device memory, so the host is not involved between rounds (the pages
-// note the ten sequential rounds set the latency floor).
+// point out that rounds which must run one after another bound the latency from below).
 #include "jepa_cem.h"
 #include "common.cuh"
 

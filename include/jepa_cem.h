@@ -8,7 +8,8 @@
  * model where each one leads, measures how far each predicted embedding lies from the
  * goal embedding and refits the Gaussian to the K closest; the caller receives only
  * the first action of the closest sequence of the last round. Section "Measured on 8x A100" adds that the
- * predictor is frame-causal (so a KV cache across rollout steps is exact), that it
+ * predictor attends only to current and earlier frames (so keys and values cached between
+ * rollout steps stay exact), that it
  * runs in bf16 with flash attention, and that the same seed gives the same plan
  * however the candidates are batched.
  *

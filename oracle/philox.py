@@ -5,9 +5,9 @@ definition of Philox (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
 Easy as 1, 2, 3", SC'11): a 4x32-bit counter and a 2x32-bit key, ten rounds of
 two 32x32->64 multiplies with the key bumped by the Weyl constants between rounds.
 
-The planning page says only that CEM draws its candidate action sequences from a
-Gaussian around the current guess (section "Where the sixteen seconds actually
-goes") and that the same seeds give identical plans at every GPU count
+The planning page says only that CEM samples its candidates from a Gaussian
+around the current guess (section "Where the sixteen seconds actually
+goes") and that a given seed yields the same plan whatever the number of GPUs
 (section "Measured on 8x A100"). Reading taken (ours): every draw is addressed by
 (candidate n, problem b, round r, quad q) so no draw depends on how candidates
 are batched or sharded:

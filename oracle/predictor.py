@@ -3,8 +3,9 @@
 Test infrastructure (see the package docstring). float64 numpy throughout.
 
 The planning page fixes what the predictor is used for: it is frame-causal
-(section "Measured on 8x A100": a KV cache across rollout steps is exact, since the
-frames already processed do not change), it rolls forward step by step over the
+(section "Measured on 8x A100": cached keys and values stay exact between rollout
+steps, since the frames already processed do not change), it advances one frame at
+a time across the
 horizon (section "E. Serving-level optimization"), and each rollout is scored
 against the goal embedding (section "Where the sixteen seconds actually goes").
 It gives no internals; the shapes come from the synthetic configurations and the

@@ -66,7 +66,7 @@ def test_small_bf16_matches_oracle(B, N, H):
 
 def test_chunk_permutation_and_batch_invariance():
     """Same candidates give bitwise-identical energies however they are chunked, ordered or
-    batched with other problems (the planning page: identical plans at 1, 2, 4 and 8 GPUs)."""
+    batched with other problems (the planning page reports the same plans for GPU counts from one to eight)."""
     pc = synthetic.SMALL
     B, N, H = 2, 40, 2
     z0, goal, s0, acts = _inputs(pc, B, N, H, seed=5)

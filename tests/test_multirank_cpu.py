@@ -1,7 +1,7 @@
 """The multi-process path of bench.py on CPU (world size 2, gloo, 127.0.0.1): problems are
 sharded across ranks with no collective on the data path, each rank plans its own, and the
 plans gathered from the ranks equal the single-process plans bit for bit (the planning page:
-the same seeds give identical plans at every GPU count). The planner here is the oracle, so
+a given seed yields the same plan whatever the number of GPUs). The planner here is the oracle, so
 the test needs no GPU; the timing reduction is the one bench.py uses."""
 import os
 import socket
