@@ -300,3 +300,76 @@ def test_energy_closed_form():
     g = rng.standard_normal((5, 6))
     z = np.stack([g + 0.25, g - 0.5, g])
     assert np.allclose(predictor.energy_l1(z, g), [0.25, 0.5, 0.0], atol=1e-15)
+
+
+def _embed_by_loops(w, z, a, s):
+    """Frame-block tokens written out one token and one output channel at a time.
+
+    Token 0 embeds the action, token 1 the state, tokens 2.. embed the P context patches;
+    every token then gets the learned position of its index within the block."""
+    n, P, E = z.shape
+    d = w["pos"].shape[1]
+    out = np.zeros((n, P + 2, d))
+    for i in range(n):
+        for t in range(P + 2):
+            for c in range(d):
+                if t == 0:
+                    v = w["b_a"][c] + sum(w["W_a"][c, j] * a[i, j] for j in range(a.shape[1]))
+                elif t == 1:
+                    v = w["b_s"][c] + sum(w["W_s"][c, j] * s[i, j] for j in range(s.shape[1]))
+                else:
+                    v = w["b_in"][c] + sum(w["W_in"][c, e] * z[i, t - 2, e] for e in range(E))
+                out[i, t, c] = v + w["pos"][t, c]
+    return out
+
+
+def test_embed_block_equals_per_token_loops():
+    """The frame-block embedding against an explicit loop over candidates, tokens and channels
+    (a dropped bias, a position added to only some tokens, or swapped action / state slots all
+    change some entry)."""
+    cfg = synthetic.PredictorConfig("embed", layers=1, width=6, heads=2, mlp=8, patch_tokens=3,
+                                    embed_dim=4, precision="fp32")
+    w = _w(cfg, seed=20)
+    rng = np.random.default_rng(21)
+    z = rng.standard_normal((2, cfg.patch_tokens, cfg.embed_dim))
+    a, s = rng.uniform(-1, 1, (2, 7)), rng.standard_normal((2, 7))
+    got = predictor.embed_block(w, z, a, s)
+    assert got.shape == (2, cfg.tokens, cfg.width)
+    assert np.allclose(got, _embed_by_loops(w, z, a, s), rtol=1e-13, atol=1e-14)
+
+
+def test_embed_block_zero_weight_probes():
+    """Probes with zeroed parts of the embedding, each isolating one term:
+    W_in = W_a = W_s = 0 leaves bias + position per slot; pos = 0 with only one slot's bias
+    non-zero lights up exactly that slot; unit inputs read one column of each matrix into
+    its own slot, in the order [action, state, patches]."""
+    cfg = synthetic.PredictorConfig("embed", layers=1, width=5, heads=1, mlp=4, patch_tokens=2,
+                                    embed_dim=3, precision="fp32")
+    w = _w(cfg, seed=22)
+    rng = np.random.default_rng(23)
+    z = rng.standard_normal((1, 2, 3))
+    a, s = rng.uniform(-1, 1, (1, 7)), rng.standard_normal((1, 7))
+    zero = {k: np.zeros_like(w[k]) for k in ("W_in", "W_a", "W_s")}
+    x = predictor.embed_block(dict(w, **zero), z, a, s)[0]
+    assert np.allclose(x[0], w["b_a"] + w["pos"][0], atol=1e-15)
+    assert np.allclose(x[1], w["b_s"] + w["pos"][1], atol=1e-15)
+    for p in range(2):
+        assert np.allclose(x[2 + p], w["b_in"] + w["pos"][2 + p], atol=1e-15)
+    # one bias at a time, positions and matrices off: only that slot is non-zero
+    off = dict(w, **zero, pos=np.zeros_like(w["pos"]),
+               b_a=np.zeros_like(w["b_a"]), b_s=np.zeros_like(w["b_s"]), b_in=np.zeros_like(w["b_in"]))
+    for name, slots in (("b_a", [0]), ("b_s", [1]), ("b_in", [2, 3])):
+        x = predictor.embed_block(dict(off, **{name: np.arange(1.0, 6.0)}), z, a, s)[0]
+        for t in range(4):
+            assert np.array_equal(x[t], np.arange(1.0, 6.0) if t in slots else np.zeros(5)), (name, t)
+    # unit inputs: action e_2 gives column 2 of W_a in slot 0, state e_4 column 4 of W_s in
+    # slot 1, and patch p = e_p gives column p of W_in in slot 2 + p
+    bare = dict(w, pos=np.zeros_like(w["pos"]), b_a=np.zeros_like(w["b_a"]),
+                b_s=np.zeros_like(w["b_s"]), b_in=np.zeros_like(w["b_in"]))
+    ea, es, ez = np.zeros((1, 7)), np.zeros((1, 7)), np.zeros((1, 2, 3))
+    ea[0, 2], es[0, 4], ez[0, 0, 0], ez[0, 1, 1] = 1.0, 1.0, 1.0, 1.0
+    x = predictor.embed_block(bare, ez, ea, es)[0]
+    assert np.array_equal(x[0], w["W_a"][:, 2])
+    assert np.array_equal(x[1], w["W_s"][:, 4])
+    assert np.array_equal(x[2], w["W_in"][:, 0])
+    assert np.array_equal(x[3], w["W_in"][:, 1])
