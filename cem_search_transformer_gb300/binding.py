@@ -128,6 +128,39 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
+_DTYPES = {"f32": ("float32",), "bf16": ("bfloat16", "int16", "uint16"), "u8": ("uint8", "float8_e4m3fn"),
+           "i32": ("int32",), "u32": ("int32", "uint32")}
+
+
+def _arg(t, name: str, kind: str, numel: int, host_ok: bool = False,
+         optional: bool = False) -> Optional[int]:
+    """Address of argument `t` after checking that it can hold `numel` elements of `kind`.
+
+    A torch tensor must have that element type, be contiguous, hold at least `numel`
+    elements and live on a CUDA device (or, where `host_ok`, in host memory); anything else
+    raises JepaError(INVALID_ARG) before the library is called, so that no kernel reads or
+    writes past a caller's buffer. A raw integer address is passed through unchecked: the
+    caller vouches for its size and location. None is allowed only for optional arguments."""
+    if t is None:
+        if optional:
+            return None
+        raise JepaError(1, f"{name} is required")
+    if isinstance(t, int):
+        return t
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise JepaError(1, f"{name}: expected a torch tensor or an integer address, got {type(t).__name__}")
+    if str(t.dtype).replace("torch.", "") not in _DTYPES[kind]:
+        raise JepaError(1, f"{name}: dtype {t.dtype} where {kind} is required")
+    if not t.is_contiguous():
+        raise JepaError(1, f"{name} must be contiguous")
+    if not t.is_cuda and not host_ok:
+        raise JepaError(1, f"{name} must be a CUDA tensor")
+    if t.numel() < numel:
+        raise JepaError(1, f"{name} holds {t.numel()} elements, {numel} are needed")
+    return t.data_ptr()
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -142,9 +175,13 @@ def energy_l1_noalloc(z_pred, goal, B, N, P, E, energy, stream=None):
     framework, or a control loop that must not allocate mid-episode). Raises JepaError with
     the library's message on failure, e.g. when B*N*ceil(P/32) exceeds the fixed scratch."""
     lib = load()
+    if min(B, N, P, E) < 1:
+        raise JepaError(1, "energy_l1_noalloc: B, N, P and E must be positive")
+    zp = _arg(z_pred, "z_pred", "f32", B * N * P * E)
+    gp = _arg(goal, "goal", "f32", B * P * E)
+    ep = _arg(energy, "energy", "f32", B * N)
     buf = ctypes.create_string_buffer(256)
-    st = lib.jepa_energy_l1_noalloc(_ptr(z_pred), _ptr(goal), B, N, P, E, _ptr(energy),
-                                    _stream(stream), buf, len(buf))
+    st = lib.jepa_energy_l1_noalloc(zp, gp, B, N, P, E, ep, _stream(stream), buf, len(buf))
     if st != JEPA_OK:
         raise JepaError(st, buf.value.decode())
 
@@ -190,55 +227,103 @@ class Planner:
         buf = ctypes.create_string_buffer(blob, len(blob))
         return self.lib.jepa_load_weights(self.h, buf, len(blob))
 
+    def _dims(self, **sizes):
+        for k, v in sizes.items():
+            if int(v) < 1:
+                raise JepaError(1, f"{k} must be >= 1 (got {v})")
+
     def sample_actions(self, mu, sigma, B, N, H, rnd, seed, actions, stream=None):
-        self._check(self.lib.jepa_sample_actions(self.h, _ptr(mu), _ptr(sigma), B, N, H, rnd, seed,
-                                                 _ptr(actions), _stream(stream)), "sample_actions")
+        self._dims(B=B, N=N, H=H)
+        A = self.pc.action_dim
+        self._check(self.lib.jepa_sample_actions(
+            self.h, _arg(mu, "mu", "f32", B * H * A), _arg(sigma, "sigma", "f32", B * H * A), B, N,
+            H, rnd, seed, _arg(actions, "actions", "f32", B * N * H * A), _stream(stream)),
+            "sample_actions")
 
     def philox(self, counters, seed, n, out, stream=None):
-        self._check(self.lib.jepa_philox4x32_10(self.h, _ptr(counters), seed, n, _ptr(out),
+        self._dims(n=n)
+        self._check(self.lib.jepa_philox4x32_10(self.h, _arg(counters, "counters", "u32", 4 * n),
+                                                seed, n, _arg(out, "out", "u32", 4 * n),
                                                 _stream(stream)), "philox4x32_10")
 
     def predictor_forward(self, z_ctx, state0, actions, B, N, H, goal=None, z_pred=None,
                           energy=None, stream=None):
+        self._dims(B=B, N=N, H=H)
+        pc, PE = self.pc, self.pc.patch_tokens * self.pc.embed_dim
         self._check(self.lib.jepa_predictor_forward(
-            self.h, _ptr(z_ctx), _ptr(state0), _ptr(actions), B, N, H, _ptr(goal), _ptr(z_pred),
-            _ptr(energy), _stream(stream)), "predictor_forward")
+            self.h, _arg(z_ctx, "z_ctx", "f32", B * PE), _arg(state0, "state0", "f32", B * pc.state_dim),
+            _arg(actions, "actions", "f32", B * N * H * pc.action_dim), B, N, H,
+            _arg(goal, "goal", "f32", B * PE, optional=True),
+            _arg(z_pred, "z_pred", "f32", B * N * PE, optional=True),
+            _arg(energy, "energy", "f32", B * N, optional=True), _stream(stream)), "predictor_forward")
 
     def select_refit(self, energy, actions, B, N, H, K, mu_out, sigma_out, elites_out=None,
                      stream=None):
+        self._dims(B=B, N=N, H=H, K=K)
+        HA = H * self.pc.action_dim
         self._check(self.lib.jepa_cem_select_refit(
-            self.h, _ptr(energy), _ptr(actions), B, N, H, K, _ptr(mu_out), _ptr(sigma_out),
-            _ptr(elites_out), _stream(stream)), "select_refit")
+            self.h, _arg(energy, "energy", "f32", B * N), _arg(actions, "actions", "f32", B * N * HA),
+            B, N, H, K, _arg(mu_out, "mu_out", "f32", B * HA), _arg(sigma_out, "sigma_out", "f32", B * HA),
+            _arg(elites_out, "elites_out", "i32", B * K, optional=True), _stream(stream)),
+            "select_refit")
 
     def plan(self, z0, state0, goal, mu0, sigma0, B, H, N, K, rounds, seed, action_out,
              trace: Optional[Dict[str, object]] = None, stream=None):
-        """Inputs/outputs may be torch CUDA tensors, or raw host/device addresses (int)."""
+        """Inputs and action_out may be torch tensors (CUDA or host) or raw host/device
+        addresses (int); the trace's buffers are CUDA tensors or device addresses."""
+        self._dims(B=B, H=H, N=N, K=K, rounds=rounds)
+        pc = self.pc
+        PE, HA, R = pc.patch_tokens * pc.embed_dim, H * pc.action_dim, rounds
         tr = None
         if trace is not None:
-            tr = Trace(*(_ptr(trace.get(k)) for k in ("mu", "sigma", "actions", "energy",
-                                                         "elites", "winner")))
+            sizes = {"mu": ("f32", (R + 1) * B * HA), "sigma": ("f32", (R + 1) * B * HA),
+                     "actions": ("f32", R * B * N * HA), "energy": ("f32", R * B * N),
+                     "elites": ("i32", R * B * K), "winner": ("i32", B)}
+            tr = Trace(*(_arg(trace.get(k), f"trace[{k}]", sizes[k][0], sizes[k][1], optional=True)
+                         for k in ("mu", "sigma", "actions", "energy", "elites", "winner")))
         self._check(self.lib.jepa_cem_plan(
-            self.h, _ptr(z0), _ptr(state0), _ptr(goal), _ptr(mu0), _ptr(sigma0), B, H, N, K,
-            rounds, seed, _ptr(action_out), ctypes.byref(tr) if tr is not None else None,
-            _stream(stream)), "cem_plan")
+            self.h, _arg(z0, "z0", "f32", B * PE, host_ok=True),
+            _arg(state0, "state0", "f32", B * pc.state_dim, host_ok=True),
+            _arg(goal, "goal", "f32", B * PE, host_ok=True),
+            _arg(mu0, "mu0", "f32", B * HA, host_ok=True),
+            _arg(sigma0, "sigma0", "f32", B * HA, host_ok=True), B, H, N, K, rounds, seed,
+            _arg(action_out, "action_out", "f32", B * pc.action_dim, host_ok=True),
+            ctypes.byref(tr) if tr is not None else None, _stream(stream)), "cem_plan")
 
     def warm_start(self, mu_prev, mu_prior, sigma_prior, B, H, mu_out, sigma_out, stream=None):
+        self._dims(B=B, H=H)
+        n = B * H * self.pc.action_dim
         self._check(self.lib.jepa_cem_warm_start(
-            self.h, _ptr(mu_prev), _ptr(mu_prior), _ptr(sigma_prior), B, H, _ptr(mu_out),
-            _ptr(sigma_out), _stream(stream)), "cem_warm_start")
+            self.h, _arg(mu_prev, "mu_prev", "f32", n), _arg(mu_prior, "mu_prior", "f32", n),
+            _arg(sigma_prior, "sigma_prior", "f32", n), B, H, _arg(mu_out, "mu_out", "f32", n),
+            _arg(sigma_out, "sigma_out", "f32", n), _stream(stream)), "cem_warm_start")
 
     def world_model_step(self, z, state, action, B, z_next, state_next, goal=None, distance=None,
                          stream=None):
+        self._dims(B=B)
+        pc, PE = self.pc, self.pc.patch_tokens * self.pc.embed_dim
         self._check(self.lib.jepa_world_model_step(
-            self.h, _ptr(z), _ptr(state), _ptr(action), B, _ptr(goal), _ptr(z_next),
-            _ptr(state_next), _ptr(distance), _stream(stream)), "world_model_step")
+            self.h, _arg(z, "z", "f32", B * PE), _arg(state, "state", "f32", B * pc.state_dim),
+            _arg(action, "action", "f32", B * pc.action_dim), B,
+            _arg(goal, "goal", "f32", B * PE, optional=True), _arg(z_next, "z_next", "f32", B * PE),
+            _arg(state_next, "state_next", "f32", B * pc.state_dim),
+            _arg(distance, "distance", "f32", B, optional=True), _stream(stream)), "world_model_step")
 
     def closed_loop(self, z0, state0, goal, mu_prior, sigma_prior, B, H, N, K, rounds, steps,
                     warm, seed, actions_out, distance_out, stream=None):
+        self._dims(B=B, H=H, N=N, K=K, rounds=rounds, steps=steps)
+        pc = self.pc
+        PE, HA = pc.patch_tokens * pc.embed_dim, H * pc.action_dim
         self._check(self.lib.jepa_cem_closed_loop(
-            self.h, _ptr(z0), _ptr(state0), _ptr(goal), _ptr(mu_prior), _ptr(sigma_prior), B, H,
-            N, K, rounds, steps, int(warm), seed, _ptr(actions_out), _ptr(distance_out),
-            _stream(stream)), "cem_closed_loop")
+            self.h, _arg(z0, "z0", "f32", B * PE, host_ok=True),
+            _arg(state0, "state0", "f32", B * pc.state_dim, host_ok=True),
+            _arg(goal, "goal", "f32", B * PE, host_ok=True),
+            _arg(mu_prior, "mu_prior", "f32", B * HA, host_ok=True),
+            _arg(sigma_prior, "sigma_prior", "f32", B * HA, host_ok=True), B, H, N, K, rounds, steps,
+            int(warm), seed, _arg(actions_out, "actions_out", "f32", steps * B * pc.action_dim,
+                                  host_ok=True),
+            _arg(distance_out, "distance_out", "f32", steps * B, host_ok=True), _stream(stream)),
+            "cem_closed_loop")
 
     def kernel_count(self, B, H, N, K, rounds) -> int:
         c = ctypes.c_int64()
@@ -247,23 +332,35 @@ class Planner:
         return c.value
 
     def linear_bf16(self, A, W, bias, M, N, K, gelu, out, stream=None):
-        self._check(self.lib.jepa_linear_bf16(self.h, _ptr(A), _ptr(W), _ptr(bias), M, N, K,
-                                              int(gelu), _ptr(out), _stream(stream)), "linear_bf16")
+        self._dims(M=M, N=N, K=K)
+        n_out = N // 2 if int(gelu) == 2 else N
+        self._check(self.lib.jepa_linear_bf16(
+            self.h, _arg(A, "A", "bf16", M * K), _arg(W, "W", "bf16", N * K),
+            _arg(bias, "bias", "f32", N, optional=True), M, N, K, int(gelu),
+            _arg(out, "out", "f32", M * n_out), _stream(stream)), "linear_bf16")
 
     def linear_fp8(self, A, a_scale, W, w_scale, bias, M, N, K, gelu, out, stream=None):
-        self._check(self.lib.jepa_linear_fp8(self.h, _ptr(A), _ptr(a_scale), _ptr(W), _ptr(w_scale),
-                                             _ptr(bias), M, N, K, int(gelu), _ptr(out),
-                                             _stream(stream)), "linear_fp8")
+        self._dims(M=M, N=N, K=K)
+        n_out = N // 2 if int(gelu) == 2 else N
+        self._check(self.lib.jepa_linear_fp8(
+            self.h, _arg(A, "A", "u8", M * K), _arg(a_scale, "a_scale", "f32", M),
+            _arg(W, "W", "u8", N * K), _arg(w_scale, "w_scale", "f32", N),
+            _arg(bias, "bias", "f32", N, optional=True), M, N, K, int(gelu),
+            _arg(out, "out", "f32", M * n_out), _stream(stream)), "linear_fp8")
 
     def quantize_rows_fp8(self, x, rows, cols, codes, scales, stream=None):
-        self._check(self.lib.jepa_quantize_rows_fp8(self.h, _ptr(x), rows, cols, _ptr(codes),
-                                                    _ptr(scales), _stream(stream)),
-                    "quantize_rows_fp8")
+        self._dims(rows=rows, cols=cols)
+        self._check(self.lib.jepa_quantize_rows_fp8(
+            self.h, _arg(x, "x", "f32", rows * cols), rows, cols,
+            _arg(codes, "codes", "u8", rows * cols), _arg(scales, "scales", "f32", rows),
+            _stream(stream)), "quantize_rows_fp8")
 
     def attention_bf16(self, q, kv, out, ncand, T, Lk, kv_rows, heads, d, stream=None):
-        self._check(self.lib.jepa_attention_bf16(self.h, _ptr(q), _ptr(kv), _ptr(out), ncand, T, Lk,
-                                                 kv_rows, heads, d, _stream(stream)),
-                    "attention_bf16")
+        self._dims(ncand=ncand, T=T, Lk=Lk, kv_rows=kv_rows, heads=heads, d=d)
+        self._check(self.lib.jepa_attention_bf16(
+            self.h, _arg(q, "q", "bf16", ncand * T * d), _arg(kv, "kv", "bf16", ncand * kv_rows * 2 * d),
+            _arg(out, "out", "bf16", ncand * T * d), ncand, T, Lk, kv_rows, heads, d,
+            _stream(stream)), "attention_bf16")
 
     def set_use_graphs(self, on: bool):
         self._check(self.lib.jepa_set_use_graphs(self.h, int(on)), "set_use_graphs")

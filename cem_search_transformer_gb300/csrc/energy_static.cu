@@ -14,6 +14,8 @@
 #include "jepa_cem.h"
 #include "common.cuh"
 
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -24,7 +26,14 @@ constexpr long long kMaxPartials = 1LL << 20;       // 4 MiB of fp32 scratch
 static __device__ __align__(256) float g_energy_partials[kMaxPartials];
 
 constexpr int kMaxDevices = 64;
-float* g_scratch[kMaxDevices] = {};                 // device address of the array, per device
+// Device address of the array per device, with the id of the CUDA context it was taken in:
+// after a device reset the module is loaded again in a new context, possibly elsewhere, so
+// an address taken in an earlier context is looked up afresh.
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;
+  float* ptr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
 // Block (candidate c, row block rb): sum of |z - goal| over rows [32 rb, 32 rb + 32) x E.
@@ -68,20 +77,53 @@ void set_msg(char* buf, size_t len, const char* msg) {
   if (buf && len) snprintf(buf, len, "%s", msg);
 }
 
-// Device address of the scratch array on the current device, taken once per device.
+// Driver entry points for the current context and its process-unique id (CUDA 12.0+),
+// resolved once through the runtime.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+cudaError_t current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the scratch array in the current device's context: looked up on the
+// first call in a context (cudaGetSymbolAddress, which also makes the runtime bind the
+// device's primary context) and cached until the context changes.
 cudaError_t scratch_for_current_device(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_energy_partials);
-    if (e != cudaSuccess) return e;
-    g_scratch[dev] = static_cast<float*>(p);
+  unsigned long long id = 0;
+  if (current_context_id(&id) == cudaSuccess && g_scratch[dev].ptr && g_scratch[dev].ctx_id == id) {
+    *out = g_scratch[dev].ptr;
+    return cudaSuccess;
   }
-  *out = g_scratch[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_energy_partials);
+  if (e != cudaSuccess) return e;
+  if ((e = current_context_id(&id)) != cudaSuccess) return e;
+  g_scratch[dev].ctx_id = id;
+  g_scratch[dev].ptr = static_cast<float*>(p);
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 

@@ -289,9 +289,10 @@ jepa_status jepa_profile_read(jepa_ctx* ctx, double* gemm_ms, double* gemm_flops
  *   energy [B,N]     dev   output: mean |z_pred - goal| per candidate
  *   err, err_len           optional caller buffer for a text description of a failure
  * Limits: B*N*ceil(P/32) <= 2^20, otherwise JEPA_ERR_SHAPE (split the candidates over
- * several calls). Runs on the current CUDA device. The first call on a device looks up the
- * array's device address (once per device), so make that first call before any stream
- * capture. All calls share the array: calls that can overlap on the GPU (on streams with
+ * several calls). Runs on the current CUDA device. The first call in a device's CUDA context
+ * looks up the array's device address and caches it for that context (a device reset makes a
+ * new context, and the next call looks the address up again), so make that first call before
+ * any stream capture. All calls share the array: calls that can overlap on the GPU (on streams with
  * no ordering between them) race and can return wrong energies; calls ordered on one
  * stream are safe. */
 jepa_status jepa_energy_l1_noalloc(const float* z_pred, const float* goal, int B, int N, int P,

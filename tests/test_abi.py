@@ -70,3 +70,25 @@ def test_product_path_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_binding_refuses_host_tensors_for_device_arguments():
+    """Tensor checks run before any library call: host, wrongly typed, non-contiguous or
+    short tensors never reach a kernel (needs only the library file, no GPU)."""
+    import torch
+    from cem_search_transformer_gb300 import binding
+    B, N, P, E = 1, 2, 3, 4
+    z, g, e = torch.zeros(B, N, P, E), torch.zeros(B, P, E), torch.zeros(B, N)
+    with pytest.raises(binding.JepaError, match="CUDA"):
+        binding.energy_l1_noalloc(z, g, B, N, P, E, e)
+    with pytest.raises(binding.JepaError, match="dtype"):
+        binding._arg(g.double(), "goal", "f32", B * P * E)
+    with pytest.raises(binding.JepaError, match="contiguous"):
+        binding._arg(torch.zeros(4, 3).t(), "x", "f32", 12, host_ok=True)
+    with pytest.raises(binding.JepaError, match="elements"):
+        binding._arg(g, "goal", "f32", B * P * E + 1, host_ok=True)
+    with pytest.raises(binding.JepaError, match="required"):
+        binding._arg(None, "goal", "f32", 1)
+    assert binding._arg(None, "goal", "f32", 1, optional=True) is None
+    assert binding._arg(1234, "goal", "f32", 1 << 40) == 1234       # raw address: caller's word
+    assert binding._arg(g, "goal", "f32", B * P * E, host_ok=True) == g.data_ptr()

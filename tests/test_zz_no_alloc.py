@@ -43,7 +43,22 @@ def test_noalloc_energy_matches_predictor_forward():
 
 def test_noalloc_energy_rejects_oversized_batches():
     z = torch.zeros(1, 4, device="cuda")
+    # raw addresses skip the binding's size checks, so the library's own limit answers:
+    # 2^20 candidates x 8 row blocks of 32 patches are beyond the fixed scratch, and the call
+    # is refused before anything is launched
     with pytest.raises(binding.JepaError) as ei:
-        # 2^20 candidates x 8 row blocks of 32 patches: beyond the fixed scratch
-        binding.energy_l1_noalloc(z, z, 1 << 10, 1 << 10, 256, 4, z)
+        binding.energy_l1_noalloc(z.data_ptr(), z.data_ptr(), 1 << 10, 1 << 10, 256, 4, z.data_ptr())
     assert ei.value.status == 2 and "fixed scratch" in str(ei.value)
+
+
+def test_noalloc_energy_rejects_short_buffers():
+    """Tensors too small for the stated shape are refused before the library is called."""
+    B, N, P, E = 1, 3, 40, 64
+    z = torch.zeros(B, N, P, E, device="cuda")
+    g = torch.zeros(B, P, E, device="cuda")
+    e = torch.zeros(B, N, device="cuda")
+    for args in ((z, g[:, :-1], e), (z[:, :-1], g, e), (z, g, e[:, :-1]),
+                 (z, g.to(torch.bfloat16), e), (z, g.transpose(1, 2), e)):
+        with pytest.raises(binding.JepaError) as ei:
+            binding.energy_l1_noalloc(args[0], args[1], B, N, P, E, args[2])
+        assert ei.value.status == 1
