@@ -296,12 +296,26 @@ cudaError_t sample_actions(const float* mu, const float* sigma, int B, int N, in
 // Raw generator words for counters[4i..4i+3] (test surface of the sampler's generator).
 cudaError_t philox_raw(const uint32_t* counters, uint64_t seed, int n, uint32_t* out, cudaStream_t s);
 
+// Layer-0 queries / keys / values of the frame-0 patch rows, which every candidate of a
+// problem shares (computed once per problem) and where to broadcast them. q_base [B*P, d] and
+// kv_base [B*P, 2d] in the activation type (ab bytes per element); q [ncand*T, d] and kv
+// (the layer-0 cache slot, kv_stride rows per candidate, 2d columns). q_base == nullptr: off.
+struct BaseRows {
+  const uint8_t* q_base = nullptr;
+  const uint8_t* kv_base = nullptr;
+  uint8_t* q = nullptr;
+  uint8_t* kv = nullptr;
+  long long kv_stride = 0;
+  int ab = 0;
+};
+
 // Frame-block token assembly for candidates [cand0, cand0+ncand) at rollout step k:
-// action and state tokens always; patch tokens copied from base[b] when base != null.
+// action and state tokens always; patch tokens copied from base[b] when base != null; the
+// layer-0 patch rows of q and the cache broadcast from br when br.q_base != null.
 cudaError_t assemble_block(const float* actions, const float* state0, const float* W_a,
                            const float* b_a, const float* W_s, const float* b_s, const float* pos,
                            const float* base, float* x, int cand0, int ncand, int N, int H, int k,
-                           int A, int S, int P, int d, cudaStream_t s);
+                           int A, int S, int P, int d, const BaseRows& br, cudaStream_t s);
 
 // energy[c] = sum of partial rows of candidate c / (P * E), fixed summation order.
 cudaError_t energy_finalize(const float* partial, int P, int ntiles, int ncand, float inv_count,

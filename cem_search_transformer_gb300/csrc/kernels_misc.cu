@@ -102,12 +102,20 @@ cudaError_t philox_raw(const uint32_t* counters, uint64_t seed, int n, uint32_t*
 // s_k = state0[b] + sum_{j<k} a_j. Patch rows are copied from base (W_in z0 + b_in + pos,
 // computed once per problem) for k == 0; for k >= 1 the in-projection GEMM writes them.
 // ---------------------------------------------------------------------------------
+// 16-byte copy of n16 vectors, block-strided.
+__device__ __forceinline__ void copy16(void* __restrict__ dst, const void* __restrict__ src,
+                                       long long n16) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (long long i = threadIdx.x; i < n16; i += blockDim.x) d4[i] = s4[i];
+}
+
 __global__ void k_assemble(const float* __restrict__ actions, const float* __restrict__ state0,
                            const float* __restrict__ W_a, const float* __restrict__ b_a,
                            const float* __restrict__ W_s, const float* __restrict__ b_s,
                            const float* __restrict__ pos, const float* __restrict__ base,
                            float* __restrict__ x, int cand0, int N, int H, int k, int A, int S,
-                           int P, int d) {
+                           int P, int d, BaseRows br) {
   __shared__ float a_s[32], s_s[32];
   const int lc = blockIdx.x;               // local candidate
   const int cand = cand0 + lc;
@@ -129,21 +137,28 @@ __global__ void k_assemble(const float* __restrict__ actions, const float* __res
     xr[c] = va;
     xr[d + c] = vs;
   }
-  if (base) {
-    const float4* src = reinterpret_cast<const float4*>(base + (long long)b * P * d);
-    float4* dst = reinterpret_cast<float4*>(xr + 2 * (long long)d);
-    const int n4 = P * d / 4;
-    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+  if (base) copy16(xr + 2 * (long long)d, base + (long long)b * P * d, (long long)P * d / 4);
+  if (br.q_base) {
+    // layer 0's queries, keys and values of the frame-0 patch rows, computed once for the
+    // problem: rows 2 .. T-1 of this candidate's q block and of its cache slot
+    const long long qrow = (long long)d * br.ab, kvrow = 2 * qrow;
+    copy16(br.q + ((long long)lc * T + 2) * qrow, br.q_base + (long long)b * P * qrow,
+           (long long)P * qrow / 16);
+    copy16(br.kv + ((long long)lc * br.kv_stride + 2) * kvrow, br.kv_base + (long long)b * P * kvrow,
+           (long long)P * kvrow / 16);
   }
 }
 
 cudaError_t assemble_block(const float* actions, const float* state0, const float* W_a,
                            const float* b_a, const float* W_s, const float* b_s, const float* pos,
                            const float* base, float* x, int cand0, int ncand, int N, int H, int k,
-                           int A, int S, int P, int d, cudaStream_t s) {
+                           int A, int S, int P, int d, const BaseRows& br, cudaStream_t s) {
   if (ncand <= 0) return cudaSuccess;
+  if (br.q_base && (((uintptr_t)br.q | (uintptr_t)br.kv | (uintptr_t)br.q_base |
+                     (uintptr_t)br.kv_base) & 15 || ((long long)d * br.ab) % 16))
+    return cudaErrorInvalidValue;
   k_assemble<<<ncand, 256, 0, s>>>(actions, state0, W_a, b_a, W_s, b_s, pos, base, x, cand0, N, H,
-                                   k, A, S, P, d);
+                                   k, A, S, P, d, br);
   return cudaGetLastError();
 }
 

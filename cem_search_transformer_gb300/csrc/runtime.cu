@@ -59,6 +59,10 @@ struct PlanGraph {
   float *z0 = nullptr, *goal = nullptr, *state0 = nullptr, *mu = nullptr, *sigma = nullptr;
   float *actions = nullptr, *energy = nullptr, *action_out = nullptr, *base = nullptr;
   void* z0_act = nullptr;
+  // layer 0's q / kv of the frame-0 patch rows per problem (and the LayerNorm output they
+  // come from): shared by every candidate of the problem
+  void *q_base = nullptr, *kv_base = nullptr, *xn_base = nullptr;
+  float* xs_base = nullptr;
   int *elites = nullptr, *winner = nullptr;
   uint64_t* seed = nullptr;
   std::vector<cudaEvent_t> ev_start, ev_end;
@@ -82,9 +86,12 @@ struct jepa_ctx {
   float* partial = nullptr;
   float* xs = nullptr;   // fp8 mode: row scales of the LayerNorm output in xn
   int ntiles = 0;
-  // scratch for jepa_predictor_forward (base + converted context)
+  // scratch for jepa_predictor_forward (base + converted context + layer-0 patch q / kv)
+  std::vector<void*> fw_allocs;
   float* fw_base = nullptr;
   void* fw_z = nullptr;
+  void *fw_qb = nullptr, *fw_kvb = nullptr, *fw_xnb = nullptr;
+  float* fw_xsb = nullptr;
   size_t fw_cap = 0;  // problems
   int* dev_err = nullptr;
   cudaStream_t cap_stream = nullptr;
@@ -295,9 +302,40 @@ jepa_status context_projection(jepa_ctx* ctx, const float* z, void* z_act, float
 
 // Predictor rollout + energy for all B*N candidates (chunked). base holds the frame-0
 // patch tokens per problem. Writes z_pred (last frame, fp32) and/or energy when non-null.
-jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0,
-                           const float* actions, int B, int N, int H, const float* goal,
-                           float* z_pred, float* energy, cudaStream_t s, PlanGraph* prof) {
+// LayerNorm 1 and the QKV product of layer 0 over the frame-0 patch rows base [B*P, d]: the
+// same for every candidate of a problem (only the action and state tokens differ before the
+// first attention). q_base [B*P, d] and kv_base [B*P, 2d] in the activation type; xn_base
+// and xs_base hold the LayerNorm output (and its fp8 row scales).
+jepa_status base_qkv(jepa_ctx* ctx, const float* base, int B, void* xn_base, float* xs_base,
+                     void* q_base, void* kv_base, cudaStream_t s, PlanGraph* prof) {
+  const jepa_config& c = ctx->cfg;
+  const int P = c.patch_tokens, d = c.width;
+  const LayerW& lw = ctx->w.layers[0];
+  const bool f8 = fp8_mode(ctx);
+  CK(layernorm(base, identity_map(), xn_base, f8 ? 2 : bf16_mode(ctx) ? 1 : 0, lw.ln1_g, lw.ln1_b,
+               B * P, d, c.ln_eps, s, xs_base));
+  Epilogue e = epi_base(ctx, EPI_STORE);
+  e.bias = lw.b_qkv;
+  e.out0 = q_base;
+  e.ld0 = d;
+  e.split = d;
+  e.out1 = kv_base;
+  e.ld1 = 2 * d;
+  if (f8) {
+    e.row_scale = xs_base;
+    e.col_scale = lw.s_qkv;
+  }
+  return gemm(ctx, xn_base, f8 ? (const void*)lw.W_qkv8 : lw.W_qkv, B * P, 3 * d, d, e, s, prof, f8);
+}
+
+// Predictor rollout + energy for all B*N candidates (chunked). base holds the frame-0 patch
+// tokens per problem; q_base / kv_base (or null) their layer-0 queries, keys and values
+// (base_qkv), which frame 0 then takes instead of recomputing them per candidate. Writes
+// z_pred (last frame, fp32) and/or energy when non-null.
+jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const void* q_base,
+                           const void* kv_base, const float* state0, const float* actions, int B,
+                           int N, int H, const float* goal, float* z_pred, float* energy,
+                           cudaStream_t s, PlanGraph* prof) {
   const jepa_config& c = ctx->cfg;
   const int T = tokens(ctx), P = c.patch_tokens, E = c.embed_dim, d = c.width, m = c.mlp;
   const int A = c.action_dim, S = c.state_dim, L = c.layers, heads = c.heads;
@@ -324,14 +362,28 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
         e.pos_off = 2;
         if ((st = gemm(ctx, ctx->zhat, ctx->w.W_in, nc * P, d, E, e, s, prof))) return st;
       }
+      // frame 0 with shared patch rows: layer 0 computes LayerNorm 1 and QKV for the action
+      // and state rows only; the patch rows' q / kv are broadcast from q_base / kv_base
+      const bool shared0 = k == 0 && q_base != nullptr;
+      BaseRows br;
+      if (shared0) {
+        br.q_base = (const uint8_t*)q_base;
+        br.kv_base = (const uint8_t*)kv_base;
+        br.q = (uint8_t*)ctx->q;
+        br.kv = (uint8_t*)ctx->kv;   // layer 0's slot
+        br.kv_stride = kv_stride;
+        br.ab = (int)ab;
+      }
       CK(assemble_block(actions, state0, ctx->w.W_a, ctx->w.b_a, ctx->w.W_s, ctx->w.b_s,
                         ctx->w.pos, k == 0 ? base : nullptr, ctx->x, (int)c0, nc, N, H, k, A, S,
-                        P, d, s));
+                        P, d, br, s));
       for (int l = 0; l < L; ++l) {
         const LayerW& lw = ctx->w.layers[l];
         uint8_t* kv_slot = (uint8_t*)ctx->kv + (H > 1 ? (size_t)l * kv_slot_elems * ab : 0);
-        CK(layernorm(ctx->x, identity_map(), ctx->xn, ln_out, lw.ln1_g, lw.ln1_b, rows, d,
-                     c.ln_eps, s, ctx->xs));
+        const bool two_rows = shared0 && l == 0;   // rows 0 and 1 of every candidate only
+        const int qkv_rows = two_rows ? nc * 2 : rows;
+        CK(layernorm(ctx->x, two_rows ? RowMap{2, (long long)T, 0} : identity_map(), ctx->xn, ln_out,
+                     lw.ln1_g, lw.ln1_b, qkv_rows, d, c.ln_eps, s, ctx->xs));
         {
           Epilogue e = epi_base(ctx, EPI_STORE);
           e.bias = lw.b_qkv;
@@ -340,13 +392,14 @@ jepa_status predictor_pass(jepa_ctx* ctx, const float* base, const float* state0
           e.split = d;
           e.out1 = kv_slot;
           e.ld1 = 2 * d;
-          e.map1 = RowMap{T, kv_stride, (long long)k * T};
+          e.map0 = two_rows ? RowMap{2, (long long)T, 0} : identity_map();
+          e.map1 = two_rows ? RowMap{2, kv_stride, 0} : RowMap{T, kv_stride, (long long)k * T};
           if (f8) {
             e.row_scale = ctx->xs;
             e.col_scale = lw.s_qkv;
           }
-          if ((st = gemm(ctx, ctx->xn, f8 ? (const void*)lw.W_qkv8 : lw.W_qkv, rows, 3 * d, d, e, s,
-                         prof, f8)))
+          if ((st = gemm(ctx, ctx->xn, f8 ? (const void*)lw.W_qkv8 : lw.W_qkv, qkv_rows, 3 * d, d, e,
+                         s, prof, f8)))
             return st;
         }
         if (bf16_mode(ctx)) {
@@ -432,12 +485,18 @@ jepa_status plan_body(jepa_ctx* ctx, PlanGraph* g, cudaStream_t s, PlanGraph* pr
   const size_t BN = (size_t)B * N;
   jepa_status s2;
   if ((s2 = context_projection(ctx, g->z0, g->z0_act, g->base, B, s, prof))) return s2;
+  const bool shared = N > 1;
+  if (shared && (s2 = base_qkv(ctx, g->base, B, g->xn_base, g->xs_base, g->q_base, g->kv_base, s,
+                               prof)))
+    return s2;
   for (int r = 0; r < R; ++r) {
     float* act_r = g->actions + (size_t)r * BN * HA;
     float* en_r = g->energy + (size_t)r * BN;
     CK(sample_actions(g->mu + (size_t)r * B * HA, g->sigma + (size_t)r * B * HA, B, N, H, A, r,
                       g->seed, 0, act_r, s));
-    if ((s2 = predictor_pass(ctx, g->base, g->state0, act_r, B, N, H, g->goal, nullptr, en_r,
+    if ((s2 = predictor_pass(ctx, g->base, shared ? g->q_base : nullptr,
+                             shared ? g->kv_base : nullptr, g->state0, act_r, B, N, H, g->goal,
+                             nullptr, en_r,
                              s, prof)))
       return s2;
     CK(select_refit(en_r, act_r, B, N, HA, K, g->mu + (size_t)(r + 1) * B * HA,
@@ -474,6 +533,10 @@ jepa_status build_plan(jepa_ctx* ctx, int B, int H, int N, int K, int R, PlanGra
       (st = dalloc(ctx, g->allocs, &g->action_out, (size_t)B * A * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->base, (size_t)B * P * d * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->z0_act, (size_t)B * P * E * act_bytes(ctx))) ||
+      (st = dalloc(ctx, g->allocs, &g->q_base, (size_t)B * P * d * act_bytes(ctx))) ||
+      (st = dalloc(ctx, g->allocs, &g->kv_base, (size_t)B * P * 2 * d * act_bytes(ctx))) ||
+      (st = dalloc(ctx, g->allocs, &g->xn_base, (size_t)B * P * d * act_bytes(ctx))) ||
+      (st = dalloc(ctx, g->allocs, &g->xs_base, (size_t)B * P * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->elites, (size_t)R * B * K * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->winner, (size_t)B * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->seed, 8))) {
@@ -587,8 +650,7 @@ void jepa_destroy(jepa_ctx* ctx) {
   if (ctx->w.gbias) cudaFree(ctx->w.gbias);
   if (ctx->w.q8) cudaFree(ctx->w.q8);
   if (ctx->w.q8s) cudaFree(ctx->w.q8s);
-  if (ctx->fw_base) cudaFree(ctx->fw_base);
-  if (ctx->fw_z) cudaFree(ctx->fw_z);
+  free_list(ctx->fw_allocs);
   if (ctx->dev_err) cudaFree(ctx->dev_err);
   if (ctx->cap_stream) cudaStreamDestroy(ctx->cap_stream);
   delete ctx;
@@ -842,19 +904,30 @@ jepa_status jepa_predictor_forward(jepa_ctx* ctx, const float* z_ctx, const floa
   if ((st = ensure_workspace(ctx, chunk_for(ctx, (long long)B * N), H))) return st;
   if ((size_t)B > ctx->fw_cap) {
     CK(cudaDeviceSynchronize());
-    if (ctx->fw_base) cudaFree(ctx->fw_base);
-    if (ctx->fw_z) cudaFree(ctx->fw_z);
-    ctx->fw_base = nullptr;
-    ctx->fw_z = nullptr;
+    free_list(ctx->fw_allocs);
     ctx->fw_cap = 0;
-    CK(cudaMalloc(&ctx->fw_base, (size_t)B * c.patch_tokens * c.width * 4));
-    CK(cudaMalloc(&ctx->fw_z, (size_t)B * c.patch_tokens * c.embed_dim * act_bytes(ctx)));
+    const size_t BP = (size_t)B * c.patch_tokens, d = c.width, ab = act_bytes(ctx);
+    if ((st = dalloc(ctx, ctx->fw_allocs, &ctx->fw_base, BP * d * 4)) ||
+        (st = dalloc(ctx, ctx->fw_allocs, &ctx->fw_z, BP * c.embed_dim * ab)) ||
+        (st = dalloc(ctx, ctx->fw_allocs, &ctx->fw_qb, BP * d * ab)) ||
+        (st = dalloc(ctx, ctx->fw_allocs, &ctx->fw_kvb, BP * 2 * d * ab)) ||
+        (st = dalloc(ctx, ctx->fw_allocs, &ctx->fw_xnb, BP * d * ab)) ||
+        (st = dalloc(ctx, ctx->fw_allocs, &ctx->fw_xsb, BP * 4))) {
+      free_list(ctx->fw_allocs);
+      return st;
+    }
     ctx->fw_cap = B;
   }
   cudaStream_t s = (cudaStream_t)stream;
   if ((st = context_projection(ctx, z_ctx, ctx->fw_z, ctx->fw_base, B, s, nullptr))) return st;
-  return predictor_pass(ctx, ctx->fw_base, state0, actions, B, N, H, goal, z_pred, energy, s,
-                        nullptr);
+  // with a single candidate per problem nothing is shared: the plain pass does the same work
+  const bool shared = N > 1;
+  if (shared && (st = base_qkv(ctx, ctx->fw_base, B, ctx->fw_xnb, ctx->fw_xsb, ctx->fw_qb,
+                               ctx->fw_kvb, s, nullptr)))
+    return st;
+  return predictor_pass(ctx, ctx->fw_base, shared ? ctx->fw_qb : nullptr,
+                        shared ? ctx->fw_kvb : nullptr, state0, actions, B, N, H, goal, z_pred,
+                        energy, s, nullptr);
 }
 
 jepa_status jepa_cem_select_refit(jepa_ctx* ctx, const float* energy, const float* actions, int B,

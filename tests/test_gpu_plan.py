@@ -265,13 +265,18 @@ def test_plan_errors_and_kernel_count():
     with pytest.raises(JepaError) as ei:
         p.plan(z, s, z, m, m, 1, 1, 8, 9, 1, 0, o)    # K > N
     assert ei.value.status == 1
+    m2 = torch.zeros(1, 2, 7, device="cuda")
     with pytest.raises(JepaError) as ei:
-        p.plan(z, s, z, m, m, 1, 2, 8, 2, 1, 0, o)    # H > max_horizon
+        p.plan(z, s, z, m2, m2, 1, 2, 8, 2, 1, 0, o)  # H > max_horizon
     assert ei.value.status == 2
+    with pytest.raises(JepaError) as ei:
+        p.plan(z, s, z, m, m, 1, 2, 8, 2, 1, 0, o)    # mu0 too short for H = 2: refused
+    assert ei.value.status == 1 and "mu0" in str(ei.value)
     R, L = 2, pc.layers
     per_pass = 1 + 7 * L + 3        # assemble; 7 per layer; final LN, out-projection, energy
-    # seed + context projection + R x (sample, pass, select/refit) + winner
-    assert p.kernel_count(1, 1, 64, 8, R) == 1 + 1 + R * (1 + per_pass + 1) + 1
+    # seed + context projection + layer 0's LayerNorm and QKV of the shared frame-0 patch
+    # rows + R x (sample, pass, select/refit) + winner
+    assert p.kernel_count(1, 1, 64, 8, R) == 1 + 1 + 2 + R * (1 + per_pass + 1) + 1
     p.close()
 
 

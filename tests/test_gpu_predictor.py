@@ -160,3 +160,20 @@ def test_full_gated_sampled_candidates():
     assert rel_err(en[idx], e_ref) < TOL_BF16_ENERGY_REL and np.all(np.isfinite(en))
     print(f"full_gated: energy rel err {rel_err(en[idx], e_ref):.2e}")
     p.close()
+
+
+@pytest.mark.parametrize("name,H", [("small", 2), ("tiny", 1), ("small_fp8", 1)])
+def test_shared_frame0_rows_are_exact(name, H):
+    """Frame 0's patch rows enter layer 0 identically for every candidate of a problem, so
+    their LayerNorm and QKV product are computed once per problem (N > 1) and broadcast. A
+    candidate scored alone (N = 1, every row computed per candidate) gets the same bits."""
+    pc = synthetic.PRESETS[name]
+    B, N = 2, 6
+    z0, goal, s0, acts = _inputs(pc, B, N, H, seed=13)
+    p = make_planner(name, max_horizon=H)
+    zp, en = _run(p, pc, z0, goal, s0, acts)
+    for b in range(B):
+        for i in (0, N - 1):
+            z1, e1 = _run(p, pc, z0[b:b + 1], goal[b:b + 1], s0[b:b + 1], acts[b:b + 1, i:i + 1].copy())
+            assert np.array_equal(e1[0, 0], en[b, i]) and np.array_equal(z1[0, 0], zp[b, i])
+    p.close()
