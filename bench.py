@@ -37,10 +37,14 @@ sys.path.insert(0, ROOT)
 from cem_search_transformer_gb300 import synthetic  # noqa: E402
 
 METRIC = "CEM plan-step latency (ms, 800x10) and candidate rollouts/sec, % of roofline"
-# DRAM bytes per launch of the four per-layer GEMMs (QKV, out-projection, MLP up, MLP down)
-# on the full-shape workload, from one ncu capture (profiles/gemm_attention_counters.md).
+# DRAM bytes (read + write) per launch of the four per-layer GEMMs (QKV, out-projection,
+# MLP up, MLP down) on the full-shape workload, from one ncu capture of the GEMM kernels
+# whose source hashed to GEMM_TRAFFIC_SOURCE_SHA (the first 16 hex digits of the SHA-256 of
+# gemm_tc.cu, tc_common.cuh and common.cuh, in that order). When the kernels change, the
+# hash no longer matches and the line reports no traffic until the counters are taken again.
 GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (429e6 + 1220e6, 1271e6 + 793e6, 432e6 + 1644e6,
                                    2683e6 + 834e6)
+GEMM_TRAFFIC_SOURCE_SHA = ""
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -50,6 +54,17 @@ def load_peaks():
         d = json.load(open(p))
         return d, "measured"
     return PEAK_FALLBACK, "fallback"
+
+
+def gemm_source_sha() -> str:
+    """Hash of the GEMM kernels' source (see GEMM_TRAFFIC_SOURCE_SHA)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "cem_search_transformer_gb300", "csrc")
+    for name in ("gemm_tc.cu", "tc_common.cuh", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def rank_problems(pc, B, rank):
@@ -178,58 +193,120 @@ class ClockSampler:
 _ORACLE_WEIGHTS = {}
 
 
-def cpu_baseline(wl, budget_s: float = 15.0, problem_seed: int = 1000):
-    """The CPU oracle (numpy float64) on a bounded sample of the same workload: the first
-    round's candidates, as many as fit in about budget_s seconds. Returns (rollouts/s, info)."""
-    from oracle import philox, predictor
-    pc = wl.predictor
+def _oracle_weights(pc):
+    from oracle import predictor
     if pc.name not in _ORACLE_WEIGHTS:   # prepared once per process (outside every timing)
         _ORACLE_WEIGHTS[pc.name] = predictor.prepare_weights(synthetic.make_weights(pc, seed=0),
                                                              pc.precision)
-    w = _ORACLE_WEIGHTS[pc.name]
-    z0, goal, s0 = synthetic.make_problems(pc, 1, seed_base=problem_seed)
-    mu0, sg0 = synthetic.make_gaussian(pc, 1, wl.horizon)
-    acts = philox.sample_actions(mu0[0], sg0[0], philox.sample_eps(wl.seed, 0, 0, wl.N, wl.horizon, 7))
-    t0 = time.perf_counter()
-    predictor.energy_l1(predictor.rollout(w, pc, z0[0], s0[0], acts[:1])[-1], goal[0])
-    t1 = time.perf_counter() - t0
-    n = int(max(1, min(wl.N, budget_s / max(t1, 1e-6))))
-    t0 = time.perf_counter()
-    done = 0
-    while done < n:
-        m = min(8, n - done)
-        predictor.energy_l1(predictor.rollout(w, pc, z0[0], s0[0], acts[done:done + m])[-1], goal[0])
-        done += m
-    dt = time.perf_counter() - t0
+    return _ORACLE_WEIGHTS[pc.name]
+
+
+def _oracle_cores():
     try:
         from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
     except Exception:
-        cores = os.cpu_count()
-    sample = (f"{done} candidate rollouts of round 0 (plus the select/refit, negligible) of "
-              f"{workload_desc(wl)}; numpy float64 oracle")
-    return done / dt, {"cores": cores, "sample": sample, "seconds": dt}
+        return os.cpu_count()
+
+
+class OracleSample:
+    """Round 0's candidates of a workload, rolled out and scored by the CPU oracle (numpy
+    float64): the bounded sample both CPU legs time."""
+
+    def __init__(self, wl, problem_seed: int = 1000):
+        from oracle import philox
+        self.wl, self.pc = wl, wl.predictor
+        self.w = _oracle_weights(self.pc)
+        self.z0, self.goal, self.s0 = synthetic.make_problems(self.pc, 1, seed_base=problem_seed)
+        mu0, sg0 = synthetic.make_gaussian(self.pc, 1, wl.horizon)
+        self.acts = philox.sample_actions(mu0[0], sg0[0],
+                                          philox.sample_eps(wl.seed, 0, 0, wl.N, wl.horizon, 7))
+        self.next = 0
+
+    def run(self, n: int) -> int:
+        """Rolls out and scores the next n candidates (in batches of at most 8, wrapping
+        round); returns n."""
+        from oracle import predictor
+        done = 0
+        while done < n:
+            m = min(8, n - done, self.wl.N - self.next)
+            a = self.acts[self.next:self.next + m]
+            predictor.energy_l1(predictor.rollout(self.w, self.pc, self.z0[0], self.s0[0], a)[-1],
+                                self.goal[0])
+            self.next = (self.next + m) % self.wl.N
+            done += m
+        return n
+
+    def seconds_per_rollout(self) -> float:
+        t0 = time.perf_counter()
+        self.run(1)
+        return time.perf_counter() - t0
+
+    def describe(self, n) -> str:
+        return (f"{n} candidate rollouts of round 0 (plus the select/refit, negligible) of "
+                f"{workload_desc(self.wl)}; numpy float64 oracle")
+
+
+def cpu_baseline(wl, budget_s: float = 15.0, problem_seed: int = 1000):
+    """The CPU oracle (numpy float64) on a bounded sample of the same workload: the first
+    round's candidates, as many as fit in about budget_s seconds. Returns (rollouts/s, info)."""
+    smp = OracleSample(wl, problem_seed)
+    t1 = smp.seconds_per_rollout()
+    n = int(max(1, min(wl.N, budget_s / max(t1, 1e-6))))
+    t0 = time.perf_counter()
+    smp.run(n)
+    dt = time.perf_counter() - t0
+    return n / dt, {"cores": _oracle_cores(), "sample": smp.describe(n), "seconds": dt}
+
+
+def cpu_full_configs(names=("tiny", "small")):
+    """Whole planning steps of the small configurations on the host cores (oracle cem.plan,
+    every candidate of every round): ms per step and candidate rollouts/s."""
+    from oracle import cem
+    out = {}
+    for name in names:
+        wl = synthetic.WORKLOADS[name]
+        pc = wl.predictor
+        w = synthetic.make_weights(pc, seed=0)
+        z0, goal, s0 = synthetic.make_problems(pc, 1)
+        mu0, sg0 = synthetic.make_gaussian(pc, 1, wl.horizon)
+        t0 = time.perf_counter()
+        cem.plan(w, pc, z0[0], s0[0], goal[0], mu0[0], sg0[0], wl.N, wl.K, wl.rounds, wl.seed)
+        dt = time.perf_counter() - t0
+        out[name] = {"ms_per_step": dt * 1e3, "rollouts_per_s": wl.N * wl.rounds / dt,
+                     "workload": workload_desc(wl)}
+    return out
 
 
 def run_reference(args, wl):
+    """The oracle as the reference arm: every step rolls out and scores a bounded sample of
+    the workload's round-0 candidates on the host cores; the warm-up steps take one
+    candidate each. The timed steps share a budget of --cpu-budget seconds."""
     rank, world, _ = rank_info()
     if rank != 0:
         return
-    per_step = []
-    info = None
-    for i in range(args.warmup + args.steps):
-        v, info = cpu_baseline(wl, budget_s=args.cpu_budget / max(1, args.steps))
-        if i >= args.warmup:
-            per_step.append(v)
-    value = float(np.mean(per_step))
-    steps_ms = wl.N * wl.rounds * wl.B / value * 1e3
+    smp = OracleSample(wl)
+    t1 = min(smp.seconds_per_rollout() for _ in range(max(1, args.warmup)))
+    n_step = int(max(1, min(wl.N, args.cpu_budget / max(1, args.steps) / max(t1, 1e-6))))
+    step_s = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        smp.run(n_step)
+        step_s.append(time.perf_counter() - t0)
+    value = n_step * args.steps / sum(step_s)
+    sample = smp.describe(n_step) + " per step"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "candidate rollouts/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": steps_ms, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": float(np.mean(step_s)) * 1e3,
+            "ms_per_full_step_extrapolated": wl.N * wl.rounds * wl.B / value * 1e3,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) embeddings)",
-            "config": {"workload": workload_desc(wl), "parallelism": "none (host cores)"},
-            "cpu_baseline": {"value": value, "unit": "candidate rollouts/s", "cores": info["cores"],
-                             "kind": "oracle", "sample": info["sample"]},
+            "config": {"workload": workload_desc(wl), "per_rank_problems": wl.B,
+                       "parallelism": "none (host cores)",
+                       "step": f"a bounded sample: {n_step} of the step's {wl.N * wl.rounds * wl.B} "
+                               "candidate rollouts (ms_per_step is the sample's time)"},
+            "cpu_baseline": {"value": value, "unit": "candidate rollouts/s", "cores": _oracle_cores(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "candidate rollouts/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -361,9 +438,17 @@ def run_ours(args, wl):
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": (achieved / peak) if achieved else None,
                          "peak_source": peak_source,
+                         "frac_of_measured_burst": (achieved / peaks.get("bf16_tflops", PEAK_FALLBACK["bf16_tflops"])
+                                                    if achieved and pc.precision != "fp8" else None),
+                         "frac_of_nominal_dense": (achieved / 2250.0
+                                                   if achieved and pc.precision != "fp8" else None),
+                         "sm_mhz_median": clocks.get("sm_mhz"),
                          "traffic": (sum(GEMM_DRAM_BYTES_PER_LAUNCH_FULL) / 4
-                                     if args.workload == "full" and not args.candidates else None),
+                                     if args.workload == "full" and not args.candidates
+                                     and gemm_source_sha() == GEMM_TRAFFIC_SOURCE_SHA else None),
                          "traffic_unit": "DRAM bytes per launch (mean of the four per-layer GEMMs)",
+                         "traffic_source": f"ncu capture of the GEMM source hashed {GEMM_TRAFFIC_SOURCE_SHA or '(none)'}; "
+                                           f"current source {gemm_source_sha()}",
                          "gemm_share_of_step": (gemm_ms / prof_steps) / step_ms if gemm_launches else None,
                          "gemm_tflop_per_step": step_flops / 1e12 if step_flops else None},
             "step_roofline": step_roofline(pc, H, N * R * B, step_flops / 1e12 if step_flops else None,
@@ -377,8 +462,99 @@ def run_ours(args, wl):
             v, info = cpu_baseline(wl, budget_s=args.cpu_budget)
             line["cpu_baseline"] = {"value": v, "unit": "candidate rollouts/s", "cores": info["cores"],
                                     "kind": "oracle", "sample": info["sample"]}
+            if not args.no_cpu_full_configs:
+                line["cpu_baseline"]["full_configs"] = cpu_full_configs()
         elif world > 1:
             line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    planner.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_sharded(args, wl):
+    """Strong scaling of one planning step: the B problems' candidates of every round split
+    across the ranks (cem_search_transformer_gb300.sharded), one NCCL all-gather of the
+    energies per round. The step runs through the library's per-call entry points (no plan
+    graph), so at one rank it also measures what the graph saves."""
+    import torch
+    import torch.distributed as dist
+    from cem_search_transformer_gb300 import binding, build_lib, sharded
+
+    rank, world, local = rank_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_lib.build()
+    pc = wl.predictor
+    B, N, K, R, H = wl.B, wl.N, wl.K, wl.rounds, wl.horizon
+    planner = binding.Planner(pc, max_horizon=H, device=local,
+                              max_chunk=-(-N * B // world))
+    planner.load_weights(synthetic.make_weights(pc, seed=0))
+    z0, goal, s0 = synthetic.make_problems(pc, B)
+    mu0, sg0 = synthetic.make_gaussian(pc, B, H)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hz0, hgoal, hs0, hmu, hsg = pin(z0), pin(goal), pin(s0), pin(mu0), pin(sg0)
+    hout = torch.zeros(B, pc.action_dim).pin_memory()
+    gather = sharded.torch_all_gather() if world > 1 else (lambda buf: [buf])
+    backend = sharded.CudaBackend(planner)
+
+    def step(host_io: bool):
+        if host_io:
+            ins = [x.to(dev, non_blocking=True) for x in (hz0, hs0, hgoal, hmu, hsg)]
+        else:
+            ins = dev_in
+        action, _ = sharded.plan_sharded(backend, *ins, B, H, N, K, R, wl.seed, world, rank, gather)
+        if host_io:
+            hout.copy_(action, non_blocking=True)
+        return action
+
+    dev_in = [x.to(dev) for x in (hz0, hs0, hgoal, hmu, hsg)]
+    for _ in range(args.warmup):
+        step(False)
+    planner.sync_check()
+    times = {}
+    with ClockSampler(local, args.clocks_dir) as clk:
+        for host_io in (False, True):
+            if world > 1:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                step(host_io)
+                if host_io:
+                    torch.cuda.current_stream(dev).synchronize()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                dist.barrier()
+            times[host_io] = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
+    planner.sync_check()
+    rollouts = N * R * B
+    if rank == 0:
+        launches = planner.kernel_count(B, H, N, K, R)
+        line = {
+            "metric": METRIC, "value": rollouts / (times[False] * 1e-3), "unit": "candidate rollouts/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": times[False],
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) embeddings)",
+            "config": {"workload": workload_desc(wl),
+                       "parallelism": f"candidates of every round split over {world} ranks, one "
+                                      "all-gather of B x N fp32 energies per round",
+                       "launch": "per-call entry points (no plan graph)",
+                       "l2": "not flushed: working set exceeds the 129 MB L2"},
+            "e2e": {"value": rollouts / (times[True] * 1e-3), "unit": "candidate rollouts/s",
+                    "ms_per_step": times[True],
+                    "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (hz0, hgoal, hs0, hmu, hsg)),
+                    "d2h_bytes_per_step": hout.numel() * hout.element_size()},
+            "gpu_launches": launches * args.steps,
+            "gpu_launches_note": "the plan graph's kernel count for the whole problem; a rank's "
+                                 "share of the predictor kernels is smaller, its per-round context "
+                                 "projection adds two",
+            "clocks": clk.summary(),
+        }
         print(json.dumps(line), flush=True)
     planner.close()
     if world > 1:
@@ -451,8 +627,16 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the plan's kernels directly on the stream instead of replaying "
                          "its CUDA graph (for the graph-vs-stream comparison)")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time: the cpu_baseline sample, or all timed steps of "
+                         "--impl reference together")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-full-configs", action="store_true",
+                    help="skip timing whole tiny and small planning steps with the oracle")
+    ap.add_argument("--shard", default="problems", choices=["problems", "candidates"],
+                    help="under torchrun: each rank plans its own problems (default), or every "
+                         "rank scores a slice of one problem's candidates with one all-gather of "
+                         "the energies per round")
     ap.add_argument("--clocks-dir", default="",
                     help="directory for the raw nvidia-smi samples (default: the temp directory)")
     args = ap.parse_args()
@@ -467,6 +651,8 @@ def main():
         run_closed_loop(args, wl)
     elif args.impl == "reference":
         run_reference(args, wl)
+    elif args.shard == "candidates":
+        run_sharded(args, wl)
     else:
         run_ours(args, wl)
 
