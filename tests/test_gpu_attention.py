@@ -30,7 +30,11 @@ def _from_bits(b):
                                                       (256, 1, 1, 1), (300, 1, 2, 1),
                                                       (129, 2, 3, 2), (387, 1, 2, 2),
                                                       (387, 2, 1, 1), (263, 1, 2, 3),
-                                                      (136, 2, 3, 2)])
+                                                      (136, 2, 3, 2),
+                                                      # several items per CTA; a 1-row last
+                                                      # tile; 7 key chunks
+                                                      (258, 1, 16, 24), (257, 2, 2, 3),
+                                                      (258, 3, 8, 30)])
 def test_attention_matches_oracle(planner, T, Lk_blocks, heads, ncand):
     d = heads * 64
     kv_rows = 3 * T
