@@ -38,13 +38,16 @@ from cem_search_transformer_gb300 import synthetic  # noqa: E402
 
 METRIC = "CEM plan-step latency (ms, 800x10) and candidate rollouts/sec, % of roofline"
 # DRAM bytes (read + write) per launch of the four per-layer GEMMs (QKV, out-projection,
-# MLP up, MLP down) on the full-shape workload, from one ncu capture of the GEMM kernels
-# whose source hashed to GEMM_TRAFFIC_SOURCE_SHA (the first 16 hex digits of the SHA-256 of
-# gemm_tc.cu, tc_common.cuh and common.cuh, in that order). When the kernels change, the
-# hash no longer matches and the line reports no traffic until the counters are taken again.
-GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (429e6 + 1220e6, 1271e6 + 793e6, 432e6 + 1644e6,
-                                   2683e6 + 834e6)
-GEMM_TRAFFIC_SOURCE_SHA = ""
+# MLP up, MLP down) on the full-shape workload: one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) of 512 candidates (132,096 rows, operands above the L2), scaled by
+# 800 / 512 to the 206,400 rows of a full launch (the traffic is proportional to the rows;
+# the weights are a few MB). Taken from the GEMM kernels whose source hashes to
+# GEMM_TRAFFIC_SOURCE_SHA (first 16 hex digits of the SHA-256 of gemm_tc.cu, tc_common.cuh
+# and common.cuh, in that order); when the kernels change, the line reports no traffic until
+# the counters are taken again.
+GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (433.0e6 + 1190.3e6, 1272.6e6 + 757.6e6, 437.5e6 + 1612.0e6,
+                                   2698.6e6 + 816.9e6)
+GEMM_TRAFFIC_SOURCE_SHA = "e5147ac8f30e333f"
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -324,6 +324,13 @@ cudaError_t energy_finalize(const float* partial, int P, int ntiles, int ncand, 
 // Per problem: sort (energy, index), elites = first K, refit mean / population std.
 cudaError_t select_refit(const float* energy, const float* actions, int B, int N, int HA, int K,
                          float* mu, float* sigma, int* elites, int* winner, cudaStream_t s);
+// Energy finalisation of a single-chunk pass (partials of all B*N candidates in `partial`),
+// then selection and refit per problem, in one launch. counter: B zero-initialised unsigned
+// ints, left at zero again.
+cudaError_t energy_select(const float* partial, int P, int ntiles, int B, int N, float inv_count,
+                          float* energy, const float* actions, int HA, int K, float* mu,
+                          float* sigma, int* elites, int* winner, unsigned int* counter,
+                          cudaStream_t s);
 
 // out[b, :] = actions[b, winner[b], 0, :]
 cudaError_t winner_action(const float* actions, const int* winner, int B, int N, int HA, int A,

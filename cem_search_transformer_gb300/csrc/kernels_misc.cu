@@ -102,12 +102,21 @@ cudaError_t philox_raw(const uint32_t* counters, uint64_t seed, int n, uint32_t*
 // s_k = state0[b] + sum_{j<k} a_j. Patch rows are copied from base (W_in z0 + b_in + pos,
 // computed once per problem) for k == 0; for k >= 1 the in-projection GEMM writes them.
 // ---------------------------------------------------------------------------------
-// 16-byte copy of n16 vectors, block-strided.
+// 16-byte copy of n16 vectors, block-strided, four loads in flight per thread.
 __device__ __forceinline__ void copy16(void* __restrict__ dst, const void* __restrict__ src,
                                        long long n16) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
   uint4* d4 = reinterpret_cast<uint4*>(dst);
-  for (long long i = threadIdx.x; i < n16; i += blockDim.x) d4[i] = s4[i];
+  const long long step = blockDim.x;
+  long long i = threadIdx.x;
+  for (; i + 3 * step < n16; i += 4 * step) {
+    const uint4 a = s4[i], b = s4[i + step], c = s4[i + 2 * step], e = s4[i + 3 * step];
+    d4[i] = a;
+    d4[i + step] = b;
+    d4[i + 2 * step] = c;
+    d4[i + 3 * step] = e;
+  }
+  for (; i < n16; i += step) d4[i] = s4[i];
 }
 
 __global__ void k_assemble(const float* __restrict__ actions, const float* __restrict__ state0,
@@ -121,6 +130,21 @@ __global__ void k_assemble(const float* __restrict__ actions, const float* __res
   const int cand = cand0 + lc;
   const int b = cand / N;
   const int T = P + 2;
+  // blockIdx.y: 0 = action and state tokens and the patch rows of x; 1 = the shared patch rows
+  // of q; 2, 3 = the two halves of the shared patch rows of the layer-0 cache slot
+  if (blockIdx.y > 0) {
+    const long long qrow = (long long)d * br.ab, kvrow = 2 * qrow;
+    if (blockIdx.y == 1) {
+      copy16(br.q + ((long long)lc * T + 2) * qrow, br.q_base + (long long)b * P * qrow,
+             (long long)P * qrow / 16);
+    } else {
+      const long long half = (long long)P * kvrow / 32;   // 16-byte vectors per half
+      const long long off = (blockIdx.y - 2) * half * 16;
+      copy16(br.kv + ((long long)lc * br.kv_stride + 2) * kvrow + off,
+             br.kv_base + (long long)b * P * kvrow + off, half);
+    }
+    return;
+  }
   const float* act = actions + (long long)cand * H * A;
   if (threadIdx.x < A) a_s[threadIdx.x] = act[k * A + threadIdx.x];
   if (threadIdx.x < S) {
@@ -138,15 +162,6 @@ __global__ void k_assemble(const float* __restrict__ actions, const float* __res
     xr[d + c] = vs;
   }
   if (base) copy16(xr + 2 * (long long)d, base + (long long)b * P * d, (long long)P * d / 4);
-  if (br.q_base) {
-    // layer 0's queries, keys and values of the frame-0 patch rows, computed once for the
-    // problem: rows 2 .. T-1 of this candidate's q block and of its cache slot
-    const long long qrow = (long long)d * br.ab, kvrow = 2 * qrow;
-    copy16(br.q + ((long long)lc * T + 2) * qrow, br.q_base + (long long)b * P * qrow,
-           (long long)P * qrow / 16);
-    copy16(br.kv + ((long long)lc * br.kv_stride + 2) * kvrow, br.kv_base + (long long)b * P * kvrow,
-           (long long)P * kvrow / 16);
-  }
 }
 
 cudaError_t assemble_block(const float* actions, const float* state0, const float* W_a,
@@ -154,11 +169,14 @@ cudaError_t assemble_block(const float* actions, const float* state0, const floa
                            const float* base, float* x, int cand0, int ncand, int N, int H, int k,
                            int A, int S, int P, int d, const BaseRows& br, cudaStream_t s) {
   if (ncand <= 0) return cudaSuccess;
-  if (br.q_base && (((uintptr_t)br.q | (uintptr_t)br.kv | (uintptr_t)br.q_base |
-                     (uintptr_t)br.kv_base) & 15 || ((long long)d * br.ab) % 16))
+  if (br.q_base && ((((uintptr_t)br.q | (uintptr_t)br.kv | (uintptr_t)br.q_base |
+                      (uintptr_t)br.kv_base) & 15) || ((long long)P * d * br.ab) % 32))
     return cudaErrorInvalidValue;
-  k_assemble<<<ncand, 256, 0, s>>>(actions, state0, W_a, b_a, W_s, b_s, pos, base, x, cand0, N, H,
-                                   k, A, S, P, d, br);
+  // layer 0's queries, keys and values of the frame-0 patch rows, computed once for the
+  // problem, go to rows 2 .. T-1 of every candidate's q block and cache slot (blocks y >= 1)
+  const dim3 grid(ncand, br.q_base ? 4 : 1);
+  k_assemble<<<grid, 256, 0, s>>>(actions, state0, W_a, b_a, W_s, b_s, pos, base, x, cand0, N, H,
+                                  k, A, S, P, d, br);
   return cudaGetLastError();
 }
 
@@ -427,15 +445,16 @@ __device__ __forceinline__ uint32_t orderable(float e) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void k_select_refit(const float* __restrict__ energy, const float* __restrict__ actions,
-                               int N, int HA, int K, int npow2, float* __restrict__ mu,
-                               float* __restrict__ sigma, int* __restrict__ elites,
-                               int* __restrict__ winner) {
-  extern __shared__ unsigned long long keys[];
-  const int b = blockIdx.x;
-  const float* e = energy + (long long)b * N;
+// Selection and refit of problem b by one block: keys (orderable energy bits << 32 | index)
+// bitonic-sorted in shared memory, elites = the first K, refit of the elites in fp64. The
+// energies are read through L2 (they may have been written by other blocks of the same
+// kernel, which the caller has ordered with a fence).
+__device__ void select_refit_block(const float* e, const float* __restrict__ ab, int N, int HA, int K,
+                                   int npow2, float* __restrict__ mu, float* __restrict__ sigma,
+                                   int* __restrict__ elites, int* __restrict__ winner, int b,
+                                   unsigned long long* keys) {
   for (int i = threadIdx.x; i < npow2; i += blockDim.x)
-    keys[i] = (i < N) ? (((unsigned long long)orderable(e[i]) << 32) | (unsigned)i)
+    keys[i] = (i < N) ? (((unsigned long long)orderable(__ldcg(e + i)) << 32) | (unsigned)i)
                       : 0xFFFFFFFFFFFFFFFFull;
   __syncthreads();
   for (int size = 2; size <= npow2; size <<= 1) {
@@ -459,7 +478,6 @@ __global__ void k_select_refit(const float* __restrict__ energy, const float* __
   if (threadIdx.x == 0 && winner) winner[b] = (int)(keys[0] & 0xFFFFFFFFu);
   // refit: one warp per (h, j) element
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const float* ab = actions + (long long)b * N * HA;
   for (int el = warp; el < HA; el += nw) {
     double s = 0.0;
     for (int i = lane; i < K; i += 32) s += (double)ab[(long long)(keys[i] & 0xFFFFFFFFu) * HA + el];
@@ -480,6 +498,16 @@ __global__ void k_select_refit(const float* __restrict__ energy, const float* __
   }
 }
 
+__global__ void k_select_refit(const float* __restrict__ energy, const float* __restrict__ actions,
+                               int N, int HA, int K, int npow2, float* __restrict__ mu,
+                               float* __restrict__ sigma, int* __restrict__ elites,
+                               int* __restrict__ winner) {
+  extern __shared__ unsigned long long keys[];
+  const int b = blockIdx.x;
+  select_refit_block(energy + (long long)b * N, actions + (long long)b * N * HA, N, HA, K, npow2, mu,
+                     sigma, elites, winner, b, keys);
+}
+
 cudaError_t select_refit(const float* energy, const float* actions, int B, int N, int HA, int K,
                          float* mu, float* sigma, int* elites, int* winner, cudaStream_t s) {
   int npow2 = 1;
@@ -491,6 +519,59 @@ cudaError_t select_refit(const float* energy, const float* actions, int B, int N
     if (e != cudaSuccess) return e;
   }
   k_select_refit<<<B, 1024, smem, s>>>(energy, actions, N, HA, K, npow2, mu, sigma, elites, winner);
+  return cudaGetLastError();
+}
+
+// Energy finalisation, elite selection and refit in one launch: blocks (x, b) each finalise
+// 32 candidates of problem b (one warp per candidate, the same fixed summation order as
+// k_energy_finalize), then the last block of problem b to finish, told by a per-problem
+// arrival counter, selects and refits that problem and resets its counter for the next use.
+__global__ void k_energy_select(const float* __restrict__ partial, int P, int ntiles, int N,
+                                float inv_count, float* energy, const float* __restrict__ actions,
+                                int HA, int K, int npow2, float* __restrict__ mu,
+                                float* __restrict__ sigma, int* __restrict__ elites,
+                                int* __restrict__ winner, unsigned int* __restrict__ counter) {
+  extern __shared__ unsigned long long keys[];
+  __shared__ bool last;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (n < N) {
+    const long long c = (long long)b * N + n;
+    const float* p = partial + c * P * ntiles;
+    const int cnt = P * ntiles;
+    float s = 0.f;
+    for (int i = lane; i < cnt; i += 32) s += p[i];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) energy[c] = s * inv_count;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(counter + b, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  select_refit_block(energy + (long long)b * N, actions + (long long)b * N * HA, N, HA, K, npow2, mu,
+                     sigma, elites, winner, b, keys);
+  if (threadIdx.x == 0) counter[b] = 0u;
+}
+
+cudaError_t energy_select(const float* partial, int P, int ntiles, int B, int N, float inv_count,
+                          float* energy, const float* actions, int HA, int K, float* mu,
+                          float* sigma, int* elites, int* winner, unsigned int* counter,
+                          cudaStream_t s) {
+  int npow2 = 1;
+  while (npow2 < N) npow2 <<= 1;
+  const size_t smem = (size_t)npow2 * sizeof(unsigned long long);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_energy_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid((N + 31) / 32, B);
+  k_energy_select<<<grid, 1024, smem, s>>>(partial, P, ntiles, N, inv_count, energy, actions, HA, K,
+                                           npow2, mu, sigma, elites, winner, counter);
   return cudaGetLastError();
 }
 

@@ -64,6 +64,7 @@ struct PlanGraph {
   void *q_base = nullptr, *kv_base = nullptr, *xn_base = nullptr;
   float* xs_base = nullptr;
   int *elites = nullptr, *winner = nullptr;
+  unsigned int* select_counter = nullptr;   // per problem, for the fused energy + selection
   uint64_t* seed = nullptr;
   std::vector<cudaEvent_t> ev_start, ev_end;
   std::vector<double> ev_flops;
@@ -489,6 +490,11 @@ jepa_status plan_body(jepa_ctx* ctx, PlanGraph* g, cudaStream_t s, PlanGraph* pr
   if (shared && (s2 = base_qkv(ctx, g->base, B, g->xn_base, g->xs_base, g->q_base, g->kv_base, s,
                                prof)))
     return s2;
+  // When one pass covers every candidate, its energy partials are all still in place when
+  // the pass ends: one kernel then finalises the energies, selects and refits (the pass's
+  // own finalisation is skipped).
+  const bool fused = BN <= (size_t)ctx->ws_chunk;
+  const jepa_config& c = ctx->cfg;
   for (int r = 0; r < R; ++r) {
     float* act_r = g->actions + (size_t)r * BN * HA;
     float* en_r = g->energy + (size_t)r * BN;
@@ -496,12 +502,18 @@ jepa_status plan_body(jepa_ctx* ctx, PlanGraph* g, cudaStream_t s, PlanGraph* pr
                       g->seed, 0, act_r, s));
     if ((s2 = predictor_pass(ctx, g->base, shared ? g->q_base : nullptr,
                              shared ? g->kv_base : nullptr, g->state0, act_r, B, N, H, g->goal,
-                             nullptr, en_r,
-                             s, prof)))
+                             nullptr, fused ? nullptr : en_r, s, prof)))
       return s2;
-    CK(select_refit(en_r, act_r, B, N, HA, K, g->mu + (size_t)(r + 1) * B * HA,
-                    g->sigma + (size_t)(r + 1) * B * HA, g->elites + (size_t)r * B * K,
-                    g->winner, s));
+    if (fused) {
+      CK(energy_select(ctx->partial, c.patch_tokens, ctx->ntiles, B, N,
+                       1.0f / ((float)c.patch_tokens * c.embed_dim), en_r, act_r, HA, K,
+                       g->mu + (size_t)(r + 1) * B * HA, g->sigma + (size_t)(r + 1) * B * HA,
+                       g->elites + (size_t)r * B * K, g->winner, g->select_counter, s));
+    } else {
+      CK(select_refit(en_r, act_r, B, N, HA, K, g->mu + (size_t)(r + 1) * B * HA,
+                      g->sigma + (size_t)(r + 1) * B * HA, g->elites + (size_t)r * B * K,
+                      g->winner, s));
+    }
   }
   CK(winner_action(g->actions + (size_t)(R - 1) * BN * HA, g->winner, B, N, HA, A,
                    g->action_out, s));
@@ -539,9 +551,14 @@ jepa_status build_plan(jepa_ctx* ctx, int B, int H, int N, int K, int R, PlanGra
       (st = dalloc(ctx, g->allocs, &g->xs_base, (size_t)B * P * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->elites, (size_t)R * B * K * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->winner, (size_t)B * 4)) ||
+      (st = dalloc(ctx, g->allocs, &g->select_counter, (size_t)B * 4)) ||
       (st = dalloc(ctx, g->allocs, &g->seed, 8))) {
     free_plan(g);
     return st;
+  }
+  if (cudaMemset(g->select_counter, 0, (size_t)B * 4) != cudaSuccess) {
+    free_plan(g);
+    return fail(ctx, JEPA_ERR_CUDA, "plan: counter init failed");
   }
   PlanGraph* prof = ctx->profile ? g : nullptr;
   cudaStream_t s = ctx->cap_stream;

@@ -275,8 +275,9 @@ def test_plan_errors_and_kernel_count():
     R, L = 2, pc.layers
     per_pass = 1 + 7 * L + 3        # assemble; 7 per layer; final LN, out-projection, energy
     # seed + context projection + layer 0's LayerNorm and QKV of the shared frame-0 patch
-    # rows + R x (sample, pass, select/refit) + winner
-    assert p.kernel_count(1, 1, 64, 8, R) == 1 + 1 + 2 + R * (1 + per_pass + 1) + 1
+    # rows + R x (sample, pass without its energy finalisation, fused energy + select/refit)
+    # + winner
+    assert p.kernel_count(1, 1, 64, 8, R) == 1 + 1 + 2 + R * (1 + (per_pass - 1) + 1) + 1
     p.close()
 
 
@@ -307,3 +308,23 @@ def test_plan_without_graph_is_bitwise_identical():
     for k in tr_g:
         assert np.array_equal(tr_g[k], tr_s[k]), k
     p.close()
+
+
+@pytest.mark.parametrize("name,B,N,K,R,H", [("small", 2, 40, 6, 3, 2), ("tiny", 1, 64, 8, 2, 1)])
+def test_fused_energy_select_equals_chunked_plan(name, B, N, K, R, H):
+    """A plan whose candidates fit one predictor pass finalises energies, selects and refits
+    in one kernel; a plan split into chunks of 7 candidates finalises per chunk and selects
+    separately. Same bits either way (elites, means, widths, energies, action)."""
+    pc = synthetic.PRESETS[name]
+    wl = synthetic.CemConfig(pc, B=B, N=N, K=K, rounds=R, horizon=H)
+    z0, goal, s0 = synthetic.make_problems(pc, B)
+    mu0, sg0 = synthetic.make_gaussian(pc, B, H)
+    outs = []
+    for chunk in (0, 7):
+        p = make_planner(name, max_horizon=H, max_chunk=chunk)
+        outs.append(_plan(p, pc, wl, z0, goal, s0, mu0, sg0))
+        p.close()
+    (a0, t0), (a1, t1) = outs
+    assert np.array_equal(a0, a1)
+    for k in ("energy", "elites", "mu", "sigma", "winner"):
+        assert np.array_equal(t0[k], t1[k]), k
