@@ -203,12 +203,15 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
         f.x *= rs * c1.x; f.y *= rs * c1.y; f.z *= rs * c1.z; f.w *= rs * c1.w;
         q.x *= rs * cg.x; q.y *= rs * cg.y; q.z *= rs * cg.z; q.w *= rs * cg.w;
       }
-      const float4 g = gelu4(make_float4(q.x + bg.x, q.y + bg.y, q.z + bg.z, q.w + bg.w));
+      const unsigned long long g01 = gelu2x(f2_add(f2_pack(q.x, q.y), f2_pack(bg.x, bg.y)));
+      const unsigned long long g23 = gelu2x(f2_add(f2_pack(q.z, q.w), f2_pack(bg.z, bg.w)));
+      const float2 o01 = f2_unpack(f2_mul(f2_add(f2_pack(f.x, f.y), f2_pack(b1.x, b1.y)), g01));
+      const float2 o23 = f2_unpack(f2_mul(f2_add(f2_pack(f.z, f.w), f2_pack(b1.z, b1.w)), g23));
       float* o = v + 16 * half + 4 * k;
-      o[0] = (f.x + b1.x) * g.x;
-      o[1] = (f.y + b1.y) * g.y;
-      o[2] = (f.z + b1.z) * g.z;
-      o[3] = (f.w + b1.w) * g.w;
+      o[0] = o01.x;
+      o[1] = o01.y;
+      o[2] = o23.x;
+      o[3] = o23.y;
     }
   }
   if (!active) return true;
@@ -265,11 +268,12 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         a.x *= rs * cs.x; a.y *= rs * cs.y; a.z *= rs * cs.z; a.w *= rs * cs.w;
       }
-      const float4 g = gelu4(make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w));
-      v[4 * k] = g.x;
-      v[4 * k + 1] = g.y;
-      v[4 * k + 2] = g.z;
-      v[4 * k + 3] = g.w;
+      const float2 g01 = f2_unpack(gelu2x(f2_add(f2_pack(a.x, a.y), f2_pack(b.x, b.y))));
+      const float2 g23 = f2_unpack(gelu2x(f2_add(f2_pack(a.z, a.w), f2_pack(b.z, b.w))));
+      v[4 * k] = g01.x;
+      v[4 * k + 1] = g01.y;
+      v[4 * k + 2] = g23.x;
+      v[4 * k + 3] = g23.y;
     }
     if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);   // r is free again
     store_rows32(epi, M, N, row_base, c0, v, stg_f, lane);
@@ -593,7 +597,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
     float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * C::STG;
     int acc = 0;
     uint32_t acc_phase = 0;
-    auto release = [](uint32_t bar) { mbar_arrive(bar); };
+    auto release = [](uint32_t bar) { mbar_arrive_relaxed(bar); };
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const int m0 = (t / num_n) * BM, n_blk = t % num_n;
       if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
@@ -746,7 +750,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
     float* stg = reinterpret_cast<float*>(smem + C::STG_OFF) + ew * C::STG;
     int acc = 0;
     uint32_t acc_phase = 0;
-    auto release = [](uint32_t bar) { mbar_arrive_cluster(bar); };
+    auto release = [](uint32_t bar) { mbar_arrive_cluster_relaxed(bar); };
     for (int t = cid; t < total; t += ncl) {
       const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n_blk = t % num_n;
       if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
