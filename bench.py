@@ -45,9 +45,9 @@ METRIC = "CEM plan-step latency (ms, 800x10) and candidate rollouts/sec, % of ro
 # GEMM_TRAFFIC_SOURCE_SHA (first 16 hex digits of the SHA-256 of gemm_tc.cu, tc_common.cuh
 # and common.cuh, in that order); when the kernels change, the line reports no traffic until
 # the counters are taken again.
-GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (433.0e6 + 1190.3e6, 1272.6e6 + 757.6e6, 437.5e6 + 1612.0e6,
-                                   2698.6e6 + 816.9e6)
-GEMM_TRAFFIC_SOURCE_SHA = "e5147ac8f30e333f"
+GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (433.0e6 + 1193.3e6, 1272.1e6 + 761.2e6, 437.6e6 + 1613.3e6,
+                                   2677.2e6 + 816.8e6)
+GEMM_TRAFFIC_SOURCE_SHA = "920534fdc0d7fad1"
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
