@@ -68,21 +68,30 @@ struct Cfg {
   static_assert(STAGES >= 3 && SMEM <= 232448, "shared memory budget");
 };
 
+// Residual tiles of the CTA-pair residual epilogue: 32 rows x 32 fp32 columns (4 KB, one
+// TMA box) per buffer, RES_BUFS buffers per epilogue warp.
+constexpr int RES_BUFS = 2;
+constexpr int RES_FLOATS = 32 * 32;
+
 // 2-SM tiles: a CTA pair computes 256 x 256 (each CTA 128 rows, all 256 columns in its TMEM);
-// each CTA stages its own 128 rows of A and its own 128-row half of W per K step.
+// each CTA stages its own 128 rows of A and its own 128-row half of W per K step. The
+// residual mode stages x through TMA buffers instead of a transpose buffer, with one
+// mbarrier per buffer.
 template <int MODE>
 struct Cfg2 {
   static constexpr int EW = epi_warps(MODE);
-  static constexpr int STG = stg_floats(MODE);
+  static constexpr int STG = MODE == EPI_RESID ? RES_BUFS * RES_FLOATS : stg_floats(MODE);
+  static constexpr int XBARS = MODE == EPI_RESID ? EW * RES_BUFS : 0;
   static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
   static constexpr int B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of the 256 columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int FIT = (232448 - 1024 - 16 - 5 * 8 - EW * STG * 4) / (STAGE_BYTES + 16);
+  static constexpr int FIT =
+      (232448 - 1024 - 16 - (5 + XBARS) * 8 - EW * STG * 4) / (STAGE_BYTES + 16);
   static constexpr int STAGES = FIT < 6 ? FIT : 6;
   static constexpr int TMEM_COLS = 512;         // two 256-column accumulators
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + EW * STG * 4;
-  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
+  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5 + XBARS) * 8 + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -458,6 +467,123 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
   }
 }
 
+// Residual epilogue of the CTA-pair kernel (EPI_RESID: x[r, c] += acc + bias; x fp32 with
+// the identity row map and row stride N), run by each epilogue warp over all of its tiles.
+// Global loads through L1 limit the bytes a warp can keep in flight, and x is read and
+// written once per element, so each warp moves its 32-row x 32-column chunks of x with TMA
+// instead: the chunk lands in one of RES_BUFS swizzled shared-memory buffers (loads run
+// RES_BUFS - 1 chunks ahead, across tile boundaries), each lane adds its accumulator row
+// (tcgen05.ld, thread = row) and the bias to its row of the buffer in place, and the buffer
+// leaves by a TMA store. Lane 0 issues the copies; rows past M read as zero and are not
+// stored. Returns false if a bounded wait expired.
+template <int EW, typename Release>
+__device__ __forceinline__ bool epilogue_resid_tma(const CUtensorMap* tmX, const Epilogue& epi,
+                                                   int M, int rank, int cid, int ncl, int num_n,
+                                                   int total, uint32_t tmem_base,
+                                                   const uint32_t (&tfull)[2],
+                                                   const uint32_t (&tempty)[2], Release release,
+                                                   float* bufs, uint32_t xbar0, int ew, int warp,
+                                                   int lane, volatile int* abort_flag,
+                                                   int* err_flag) {
+  constexpr int BN = 256;
+  constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp and tile
+  constexpr int NCH = SPAN / 32;             // 32-column chunks per tile
+  const int quarter = warp & 3, part = ew >> 2;
+  const int my_tiles = cid < total ? (total - 1 - cid) / ncl + 1 : 0;
+  const int nchunks = my_tiles * NCH;
+  const uint32_t buf0 = smem_u32(bufs);
+  // chunk g of this warp: tile cid + (g / NCH) ncl, columns 32 (g % NCH) of the warp's share
+  auto chunk_xy = [&](int g, int& x, int& y) {
+    const int t = cid + (g / NCH) * ncl;
+    y = (t / num_n) * 2 * BM + rank * BM + quarter * 32;
+    x = (t % num_n) * BN + part * SPAN + 32 * (g % NCH);
+  };
+  auto issue_load = [&](int g) {   // lane 0 only
+    if (g >= nchunks) return;
+    const int b = g % RES_BUFS;
+    int x, y;
+    chunk_xy(g, x, y);
+    if (y < M) {
+      mbar_expect_tx(xbar0 + 8u * b, RES_FLOATS * 4);
+      tma_load_2d(buf0 + b * RES_FLOATS * 4, tmX, x, y, xbar0 + 8u * b);
+    } else {
+      mbar_arrive(xbar0 + 8u * b);   // all 32 rows past M: nothing to load or store
+    }
+  };
+  if (lane == 0)
+    for (int g = 0; g < RES_BUFS; ++g) issue_load(g);
+  bool ok = true;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int i = 0; i < my_tiles && ok; ++i) {
+    const uint32_t tbase =
+        tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * SPAN);
+    if (!mbar_wait(tfull[acc], acc_phase, abort_flag, err_flag)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t r[32];
+    tmem_ld32_async(tbase, r);
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int g = i * NCH + j;
+      const int b = g % RES_BUFS;
+      tmem_wait(r);
+      if (j == NCH - 1) {
+        // accumulator fully read: hand it back to the MMA warp before finishing the stores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release(tempty[acc]);
+      }
+      if (!mbar_wait(xbar0 + 8u * b, (uint32_t)(g / RES_BUFS) & 1u, abort_flag, err_flag)) {
+        ok = false;
+        break;
+      }
+      int x, y;
+      chunk_xy(g, x, y);
+      // row `lane` of the buffer: 16-byte piece k at k ^ (lane & 7) (128-byte swizzle)
+      float* row = bufs + b * RES_FLOATS + lane * 32;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float4* pp = reinterpret_cast<float4*>(row + ((k ^ (lane & 7)) << 2));
+        const float4 bb = epi_bias4(epi, x + 4 * k);
+        float4 xv = *pp;
+        xv.x += __uint_as_float(r[4 * k]) + bb.x;
+        xv.y += __uint_as_float(r[4 * k + 1]) + bb.y;
+        xv.z += __uint_as_float(r[4 * k + 2]) + bb.z;
+        xv.w += __uint_as_float(r[4 * k + 3]) + bb.w;
+        *pp = xv;
+      }
+      if (j + 1 < NCH) tmem_ld32_async(tbase + 32u * (j + 1), r);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (y < M) {
+          tma_store_2d(tmX, buf0 + b * RES_FLOATS * 4, x, y);
+          bulk_commit_group();
+        }
+        // the buffer is refilled once the store has read it
+        bulk_wait_group_read<0>();
+        issue_load(g + RES_BUFS);
+      }
+      __syncwarp();
+    }
+    if (++acc == 2) acc = 0, acc_phase ^= 1u;
+  }
+  if (lane == 0) {
+    bulk_wait_group_all();
+    if (!ok) {
+      // loads may still be in flight into this CTA's shared memory: let them land
+      const unsigned long long t0 = globaltimer();
+      while (globaltimer() - t0 < 2000000ull) {
+      }
+    }
+  }
+  __syncwarp();
+  return ok;
+}
+
 // OP 0: bf16 operands (kind::f16, 64 elements of K per 128-byte row); OP 1: fp8 e4m3
 // operands (kind::f8f6f4, 128 elements per row) with per-row / per-column scales applied in
 // the epilogue. Stages hold the same bytes either way.
@@ -624,7 +750,8 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
 template <int MODE, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               int M, int N, int K, Epilogue epi, int* err_flag) {
+               const __grid_constant__ CUtensorMap tmX, int M, int N, int K, Epilogue epi,
+               int* err_flag) {
   constexpr int EW = epi_warps(MODE);
   constexpr int BN = 256;
   using C = Cfg2<MODE>;
@@ -637,7 +764,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
   const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
-  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + (2 * C::STAGES + 5) * 8);
+  const uint32_t xbar0 = bar0 + 8u * (2 * C::STAGES + 5);   // residual buffers (EPI_RESID)
+  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + (2 * C::STAGES + 5 + C::XBARS) * 8);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -659,6 +787,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
       mbar_init(tempty_bar(a), 2 * EW);   // epilogue warps of both CTAs (used in the leader)
     }
     mbar_init(teardown_bar, 1);
+    for (int b = 0; b < C::XBARS; ++b) mbar_init(xbar0 + 8u * b, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -751,13 +880,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
     int acc = 0;
     uint32_t acc_phase = 0;
     auto release = [](uint32_t bar) { mbar_arrive_cluster_relaxed(bar); };
-    for (int t = cid; t < total; t += ncl) {
-      const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n_blk = t % num_n;
-      if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
-                                       tfull_bar(acc), acc_phase, map_to_rank(tempty_bar(acc), 0),
-                                       release, stg, ew, warp, lane, abort_flag, err_flag))
-        break;
-      if (++acc == 2) acc = 0, acc_phase ^= 1u;
+    if constexpr (MODE == EPI_RESID) {
+      const uint32_t tf[2] = {tfull_bar(0), tfull_bar(1)};
+      const uint32_t te[2] = {map_to_rank(tempty_bar(0), 0), map_to_rank(tempty_bar(1), 0)};
+      epilogue_resid_tma<EW>(&tmX, epi, M, (int)rank, cid, ncl, num_n, total, tmem_base, tf, te,
+                             release, stg, xbar0 + 8u * (ew * RES_BUFS), ew, warp, lane,
+                             abort_flag, err_flag);
+    } else {
+      for (int t = cid; t < total; t += ncl) {
+        const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n_blk = t % num_n;
+        if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
+                                             tfull_bar(acc), acc_phase, map_to_rank(tempty_bar(acc), 0),
+                                             release, stg, ew, warp, lane, abort_flag, err_flag))
+          break;
+        if (++acc == 2) acc = 0, acc_phase ^= 1u;
+      }
     }
   }
   tc_fence_before();
@@ -827,13 +964,18 @@ static cudaError_t launch_tc2(const void* A, const void* W, int M, int N, int K,
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = set_max_dynamic_smem((const void*)k_gemm_tc2<MODE, OP>, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mx;
   if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, 128))
     return cudaErrorInvalidValue;
+  if (MODE == EPI_RESID) {
+    if (!make_map_f32(&mx, epi.out0, M, N, 32)) return cudaErrorInvalidValue;
+  } else {
+    mx = ma;   // unused
+  }
   const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
   const int pairs = num_sms / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  k_gemm_tc2<MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  k_gemm_tc2<MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, mx, M, N, K, epi, err_flag);
   return cudaGetLastError();
 }
 
@@ -856,8 +998,11 @@ static cudaError_t gemm_tc(const void* A, const void* W, int M, int N, int K, co
     if (epi.mode == EPI_STORE) return launch_tc2<EPI_STORE, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
     if (epi.mode == EPI_GELU) return launch_tc2<EPI_GELU, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
     if (epi.mode == EPI_GATED) return launch_tc2<EPI_GATED, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
+    // the residual epilogue moves x with TMA: identity row map, row stride N, 16-byte base
     if constexpr (OP == 0)
-      if (epi.mode == EPI_RESID) return launch_tc2<EPI_RESID, 0>(A, W, M, N, K, epi, err_flag, num_sms, s);
+      if (epi.mode == EPI_RESID && epi.ld0 == N && epi.map0.goff == 0 && epi.map0.rpg >= M &&
+          (((uintptr_t)epi.out0) & 15) == 0)
+        return launch_tc2<EPI_RESID, 0>(A, W, M, N, K, epi, err_flag, num_sms, s);
   }
   if (tile_n(N) == 256) return launch_mode<256, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
   return launch_mode<128, OP>(A, W, M, N, K, epi, err_flag, num_sms, s);
