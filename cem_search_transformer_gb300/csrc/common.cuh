@@ -78,6 +78,9 @@ struct Epilogue {
   // (activation row scale, weight output-channel scale) before the bias
   const float* row_scale;
   const float* col_scale;
+  // set by the CTA-pair launcher only: 1 when bf16 out0 (identity rows) leaves the GELU and
+  // gated epilogues by TMA stores through the kernel's output tensor map
+  int tma_out;
 };
 
 // GELU with the Gaussian CDF written through erf: x * (1 + erf(x / sqrt 2)) / 2.

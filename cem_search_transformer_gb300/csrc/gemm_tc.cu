@@ -80,7 +80,9 @@ constexpr int RES_FLOATS = 32 * 32;
 template <int MODE>
 struct Cfg2 {
   static constexpr int EW = epi_warps(MODE);
-  static constexpr int STG = MODE == EPI_RESID ? RES_BUFS * RES_FLOATS : stg_floats(MODE);
+  static constexpr int STG = MODE == EPI_RESID ? RES_BUFS * RES_FLOATS
+                             : MODE == EPI_STORE ? 512   // bf16 rows, as GELU
+                                                 : stg_floats(MODE);
   static constexpr int XBARS = MODE == EPI_RESID ? EW * RES_BUFS : 0;
   static constexpr int A_BYTES = BM * BK * 2;   // 16 KB
   static constexpr int B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of the 256 columns
@@ -106,13 +108,14 @@ struct Cfg2 {
 // lane i holding row row_base + i in v[0..31]. bf16 output goes through the warp's staging
 // buffer (32 rows x 64 B, 16-byte pieces swizzled by row) so that the global stores are
 // row-contiguous; fp32 output (the C-ABI linear layer) is stored row by row.
-__device__ __forceinline__ bool store_rows32(const Epilogue& epi, int M, int N, int row_base,
-                                             int c0, const float (&v)[32], float* stg_f,
-                                             int lane) {
+__device__ __forceinline__ bool store_rows32(void* out, long long ld, const RowMap& map,
+                                             int act_bf16, int M, int N, int row_base, int c0,
+                                             const float (&v)[32], float* stg_f, int lane,
+                                             const CUtensorMap* tmO, bool drain) {
   const int row = row_base + lane;
-  if (!epi.act_bf16) {
+  if (!act_bf16) {
     if (row < M) {
-      float* orow = reinterpret_cast<float*>(epi.out0) + map_row(epi.map0, row) * epi.ld0;
+      float* orow = reinterpret_cast<float*>(out) + map_row(map, row) * ld;
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         if (c0 + 4 * k < N)
@@ -122,7 +125,13 @@ __device__ __forceinline__ bool store_rows32(const Epilogue& epi, int M, int N, 
     return true;
   }
   uint8_t* stg = reinterpret_cast<uint8_t*>(stg_f);
-  // row `lane`, 16-byte piece q (8 columns) at byte lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)
+  if (drain) {
+    // the buffer is rewritten once an earlier chunk's TMA store has read it
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+  }
+  // row `lane`, 16-byte piece q (8 columns) at byte lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4),
+  // which is the 64-byte swizzle of a 32 x 32 bf16 TMA box
   const int swz = (lane >> 1) & 3;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -137,6 +146,15 @@ __device__ __forceinline__ bool store_rows32(const Epilogue& epi, int M, int N, 
     u.w = *reinterpret_cast<uint32_t*>(&h3);
     *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ swz) << 4)) = u;
   }
+  if (tmO) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row_base < M) {
+      tma_store_2d(tmO, smem_u32(stg), c0, row_base);
+      bulk_commit_group();
+    }
+    return true;
+  }
   __syncwarp();
   // 128 pieces of 16 bytes; lane takes pieces lane + 32 i: rows (lane >> 2) + 8 i, piece lane & 3
   const int q = lane & 3;
@@ -147,7 +165,7 @@ __device__ __forceinline__ bool store_rows32(const Epilogue& epi, int M, int N, 
     const int grow = row_base + rr;
     const int col = c0 + 8 * q;
     if (grow < M && col < N) {
-      bf16* dst = reinterpret_cast<bf16*>(epi.out0) + map_row(epi.map0, grow) * epi.ld0 + col;
+      bf16* dst = reinterpret_cast<bf16*>(out) + map_row(map, grow) * ld + col;
       if (col + 8 <= N) {
         *reinterpret_cast<uint4*>(dst) = u;
       } else {                                // N % 8 == 4: the last 4 columns
@@ -170,7 +188,7 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
                                                     uint32_t tfull_parity, uint32_t tempty,
                                                     Release release, float* stg_f, int ew,
                                                     int warp, int lane, volatile int* abort_flag,
-                                                    int* err_flag) {
+                                                    int* err_flag, const CUtensorMap* tmO) {
   static_assert(EW == 16, "one FC1/gate block pair per epilogue warp");
   const int quarter = warp & 3;
   const int part = ew >> 2;                  // block pair within the 256-column tile
@@ -224,22 +242,25 @@ __device__ __forceinline__ bool epilogue_tile_gated(const Epilogue& epi, int M, 
     }
   }
   if (!active) return true;
-  return store_rows32(epi, M, N, m0 + quarter * 32, ocol, v, stg_f, lane);
+  return store_rows32(epi.out0, epi.ld0, epi.map0, epi.act_bf16, M, N, m0 + quarter * 32, ocol, v,
+                      stg_f, lane, tmO, tmO != nullptr);
 }
 
-// GELU epilogue (EPI_GELU): each lane owns one accumulator row. Bias and GELU are applied in
-// that layout straight from TMEM (the bias is the same for every lane: broadcast loads), and
-// only the bf16 results go through the warp's staging buffer (32 rows x 64 B, 16-byte pieces
-// swizzled by row) so that the global stores are row-contiguous. Staging bf16 instead of
-// fp32 halves the buffer, which leaves room for one more stage of the operand ring. With
-// fp32 output (the C-ABI linear layer) rows are stored directly.
-template <int BN, int EW, int OP, typename Release>
-__device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, int N, int m0,
+// Row-per-lane epilogue (EPI_GELU; EPI_STORE in the CTA-pair kernel): each lane owns one
+// accumulator row. Bias (and GELU) are applied in that layout straight from TMEM (the bias is
+// the same for every lane: broadcast loads), and only the bf16 results go through the warp's
+// staging buffer (32 rows x 64 B, 16-byte pieces swizzled by row), from which a TMA store
+// (out0 with identity rows, when the launcher made its tensor map) or row-contiguous
+// global stores write them. Staging bf16 instead of fp32 halves the buffer, which leaves
+// room for one more stage of the operand ring. With fp32 output (the C-ABI linear layer)
+// rows are stored directly. A STORE chunk goes to out0 or out1 by its columns (split).
+template <int BN, int EW, int OP, bool GELU, typename Release>
+__device__ __forceinline__ bool epilogue_tile_rows(const Epilogue& epi, int M, int N, int m0,
                                                    int n_blk, uint32_t tmem_acc, uint32_t tfull,
                                                    uint32_t tfull_parity, uint32_t tempty,
                                                    Release release, float* stg_f, int ew, int warp,
                                                    int lane, volatile int* abort_flag,
-                                                   int* err_flag) {
+                                                   int* err_flag, const CUtensorMap* tmO) {
   const int quarter = warp & 3;
   const int part = ew >> 2;
   constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp
@@ -277,15 +298,27 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         a.x *= rs * cs.x; a.y *= rs * cs.y; a.z *= rs * cs.z; a.w *= rs * cs.w;
       }
-      const float2 g01 = f2_unpack(gelu2x(f2_add(f2_pack(a.x, a.y), f2_pack(b.x, b.y))));
-      const float2 g23 = f2_unpack(gelu2x(f2_add(f2_pack(a.z, a.w), f2_pack(b.z, b.w))));
+      unsigned long long x01 = f2_add(f2_pack(a.x, a.y), f2_pack(b.x, b.y));
+      unsigned long long x23 = f2_add(f2_pack(a.z, a.w), f2_pack(b.z, b.w));
+      if constexpr (GELU) {
+        x01 = gelu2x(x01);
+        x23 = gelu2x(x23);
+      }
+      const float2 g01 = f2_unpack(x01), g23 = f2_unpack(x23);
       v[4 * k] = g01.x;
       v[4 * k + 1] = g01.y;
       v[4 * k + 2] = g23.x;
       v[4 * k + 3] = g23.y;
     }
     if (j + 1 < nvalid) tmem_ld32_async(tbase + 32u * (j + 1), r);   // r is free again
-    store_rows32(epi, M, N, row_base, c0, v, stg_f, lane);
+    // a chunk goes wholly to out0 or to out1 (split is a multiple of 32); only out0 may have
+    // an output tensor map
+    if (c0 >= epi.split)
+      store_rows32(epi.out1, epi.ld1, epi.map1, epi.act_bf16, M, N - epi.split, row_base,
+                   c0 - epi.split, v, stg_f, lane, nullptr, tmO != nullptr);
+    else
+      store_rows32(epi.out0, epi.ld0, epi.map0, epi.act_bf16, M, N, row_base, c0, v, stg_f, lane,
+                   tmO, tmO != nullptr);
   }
   if (nvalid == 0) {
     tc_fence_before();
@@ -295,19 +328,26 @@ __device__ __forceinline__ bool epilogue_tile_gelu(const Epilogue& epi, int M, i
   return true;
 }
 
-template <int BN, int MODE, int EW, int OP, typename Release>
+template <int BN, int MODE, int EW, int OP, bool PAIR, typename Release>
 __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N, int m0, int n_blk,
                                               uint32_t tmem_acc, uint32_t tfull,
                                               uint32_t tfull_parity, uint32_t tempty,
                                               Release release, float* stg, int ew, int warp,
-                                              int lane, volatile int* abort_flag, int* err_flag) {
+                                              int lane, volatile int* abort_flag, int* err_flag,
+                                              const CUtensorMap* tmO = nullptr) {
   if constexpr (MODE == EPI_GATED) {
     static_assert(BN == 256, "gated tiles hold four FC1/gate block pairs");
     return epilogue_tile_gated<EW, OP>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
-                                       tempty, release, stg, ew, warp, lane, abort_flag, err_flag);
+                                       tempty, release, stg, ew, warp, lane, abort_flag, err_flag,
+                                       tmO);
   } else if constexpr (MODE == EPI_GELU) {
-    return epilogue_tile_gelu<BN, EW, OP>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
-                                          tempty, release, stg, ew, warp, lane, abort_flag, err_flag);
+    return epilogue_tile_rows<BN, EW, OP, true>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
+                                                 tempty, release, stg, ew, warp, lane, abort_flag,
+                                                 err_flag, tmO);
+  } else if constexpr (MODE == EPI_STORE && PAIR) {
+    return epilogue_tile_rows<BN, EW, OP, false>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
+                                                  tempty, release, stg, ew, warp, lane, abort_flag,
+                                                  err_flag, tmO);
   } else {
   const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
   const int part = ew >> 2;                  // which share of the tile's columns
@@ -726,7 +766,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
     auto release = [](uint32_t bar) { mbar_arrive_relaxed(bar); };
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const int m0 = (t / num_n) * BM, n_blk = t % num_n;
-      if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
+      if (!epilogue_tile<BN, MODE, EW, OP, false>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
                                        tfull_bar(acc), acc_phase, tempty_bar(acc), release, stg, ew,
                                        warp, lane, abort_flag, err_flag))
         break;
@@ -887,14 +927,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
                              release, stg, xbar0 + 8u * (ew * RES_BUFS), ew, warp, lane,
                              abort_flag, err_flag);
     } else {
+      const CUtensorMap* tmO = epi.tma_out ? &tmX : nullptr;
       for (int t = cid; t < total; t += ncl) {
         const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n_blk = t % num_n;
-        if (!epilogue_tile<BN, MODE, EW, OP>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
+        if (!epilogue_tile<BN, MODE, EW, OP, true>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
                                              tfull_bar(acc), acc_phase, map_to_rank(tempty_bar(acc), 0),
-                                             release, stg, ew, warp, lane, abort_flag, err_flag))
+                                             release, stg, ew, warp, lane, abort_flag, err_flag, tmO))
           break;
         if (++acc == 2) acc = 0, acc_phase ^= 1u;
       }
+      if (tmO && lane == 0) bulk_wait_group_all();   // TMA stores done before the CTA exits
     }
   }
   tc_fence_before();
@@ -967,15 +1009,25 @@ static cudaError_t launch_tc2(const void* A, const void* W, int M, int N, int K,
   CUtensorMap ma, mb, mx;
   if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, 128))
     return cudaErrorInvalidValue;
+  Epilogue ek = epi;
+  ek.tma_out = 0;
   if (MODE == EPI_RESID) {
     if (!make_map_f32(&mx, epi.out0, M, N, 32)) return cudaErrorInvalidValue;
+  } else if ((MODE == EPI_GELU || MODE == EPI_GATED || MODE == EPI_STORE) && epi.act_bf16 &&
+             epi.map0.goff == 0 && epi.map0.rpg >= M && (((uintptr_t)epi.out0) & 15) == 0 &&
+             (epi.ld0 % 8) == 0) {
+    // bf16 out0 rows leave by TMA stores (the staging buffer is the box's 64-byte swizzle);
+    // the columns of out0 are [0, split) in the store mode, N / 2 in the gated one
+    const int cols = MODE == EPI_GATED ? N / 2 : (MODE == EPI_STORE && epi.split < N ? epi.split : N);
+    if (!make_map_bf16_out(&mx, epi.out0, M, cols, epi.ld0)) return cudaErrorInvalidValue;
+    ek.tma_out = 1;
   } else {
     mx = ma;   // unused
   }
   const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
   const int pairs = num_sms / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  k_gemm_tc2<MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, mx, M, N, K, epi, err_flag);
+  k_gemm_tc2<MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, mx, M, N, K, ek, err_flag);
   return cudaGetLastError();
 }
 

@@ -385,6 +385,20 @@ inline bool make_map_f32(CUtensorMap* m, const void* ptr, int rows, int cols, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [rows, cols] with row stride ld elements, in boxes of 32 rows x 32 columns (64-byte
+// box rows, 64-byte swizzle: 16-byte piece q of row r at q ^ ((r >> 1) & 3)).
+inline bool make_map_bf16_out(CUtensorMap* m, const void* ptr, int rows, int cols, long long ld) {
+  PFN_encodeTiled enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The same for 8-bit elements (fp8 codes): 128-element (128-byte) rows per box.
 inline bool make_map_u8(CUtensorMap* m, const void* ptr, int rows, int cols, int box_rows,
                         int box_cols = 128) {
