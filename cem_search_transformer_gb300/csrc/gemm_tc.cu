@@ -108,10 +108,15 @@ struct Cfg2 {
 // lane i holding row row_base + i in v[0..31]. bf16 output goes through the warp's staging
 // buffer (32 rows x 64 B, 16-byte pieces swizzled by row) so that the global stores are
 // row-contiguous; fp32 output (the C-ABI linear layer) is stored row by row.
+// With a 2-D output map (tmO) the staged chunk leaves by one TMA store. With a 3-D map of the
+// K/V cache (tmC: columns, row within a block of map.rpg rows, block), the rows that lie in
+// the first row's block leave by one TMA store (clipped at the block end) and the rest, which
+// belong to the next candidate, by per-lane stores.
 __device__ __forceinline__ bool store_rows32(void* out, long long ld, const RowMap& map,
                                              int act_bf16, int M, int N, int row_base, int c0,
                                              const float (&v)[32], float* stg_f, int lane,
-                                             const CUtensorMap* tmO, bool drain) {
+                                             const CUtensorMap* tmO, bool drain,
+                                             const CUtensorMap* tmC = nullptr) {
   const int row = row_base + lane;
   if (!act_bf16) {
     if (row < M) {
@@ -155,6 +160,19 @@ __device__ __forceinline__ bool store_rows32(void* out, long long ld, const RowM
     }
     return true;
   }
+  int lsu_from = 0;   // first staged row written by per-lane stores
+  if (tmC && row_base + 32 <= M) {
+    const int blk_row = row_base % map.rpg;
+    lsu_from = map.rpg - blk_row < 32 ? map.rpg - blk_row : 32;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const long long blk = (long long)(row_base / map.rpg) * (map.gstride / map.rpg) + map.goff / map.rpg;
+      tma_store_3d(tmC, smem_u32(stg), c0, blk_row, (int)blk);
+      bulk_commit_group();
+    }
+    if (lsu_from == 32) return true;
+  }
   __syncwarp();
   // 128 pieces of 16 bytes; lane takes pieces lane + 32 i: rows (lane >> 2) + 8 i, piece lane & 3
   const int q = lane & 3;
@@ -164,7 +182,7 @@ __device__ __forceinline__ bool store_rows32(void* out, long long ld, const RowM
     const uint4 u = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((q ^ ((rr >> 1) & 3)) << 4));
     const int grow = row_base + rr;
     const int col = c0 + 8 * q;
-    if (grow < M && col < N) {
+    if (rr >= lsu_from && grow < M && col < N) {
       bf16* dst = reinterpret_cast<bf16*>(out) + map_row(map, grow) * ld + col;
       if (col + 8 <= N) {
         *reinterpret_cast<uint4*>(dst) = u;
@@ -260,7 +278,8 @@ __device__ __forceinline__ bool epilogue_tile_rows(const Epilogue& epi, int M, i
                                                    uint32_t tfull_parity, uint32_t tempty,
                                                    Release release, float* stg_f, int ew, int warp,
                                                    int lane, volatile int* abort_flag,
-                                                   int* err_flag, const CUtensorMap* tmO) {
+                                                   int* err_flag, const CUtensorMap* tmO,
+                                                   const CUtensorMap* tmC) {
   const int quarter = warp & 3;
   const int part = ew >> 2;
   constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp
@@ -315,10 +334,10 @@ __device__ __forceinline__ bool epilogue_tile_rows(const Epilogue& epi, int M, i
     // an output tensor map
     if (c0 >= epi.split)
       store_rows32(epi.out1, epi.ld1, epi.map1, epi.act_bf16, M, N - epi.split, row_base,
-                   c0 - epi.split, v, stg_f, lane, nullptr, tmO != nullptr);
+                   c0 - epi.split, v, stg_f, lane, nullptr, tmO != nullptr || tmC != nullptr, tmC);
     else
       store_rows32(epi.out0, epi.ld0, epi.map0, epi.act_bf16, M, N, row_base, c0, v, stg_f, lane,
-                   tmO, tmO != nullptr);
+                   tmO, tmO != nullptr || tmC != nullptr);
   }
   if (nvalid == 0) {
     tc_fence_before();
@@ -334,7 +353,8 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
                                               uint32_t tfull_parity, uint32_t tempty,
                                               Release release, float* stg, int ew, int warp,
                                               int lane, volatile int* abort_flag, int* err_flag,
-                                              const CUtensorMap* tmO = nullptr) {
+                                              const CUtensorMap* tmO = nullptr,
+                                              const CUtensorMap* tmC = nullptr) {
   if constexpr (MODE == EPI_GATED) {
     static_assert(BN == 256, "gated tiles hold four FC1/gate block pairs");
     return epilogue_tile_gated<EW, OP>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
@@ -343,11 +363,11 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
   } else if constexpr (MODE == EPI_GELU) {
     return epilogue_tile_rows<BN, EW, OP, true>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
                                                  tempty, release, stg, ew, warp, lane, abort_flag,
-                                                 err_flag, tmO);
+                                                 err_flag, tmO, nullptr);
   } else if constexpr (MODE == EPI_STORE && PAIR) {
     return epilogue_tile_rows<BN, EW, OP, false>(epi, M, N, m0, n_blk, tmem_acc, tfull, tfull_parity,
                                                   tempty, release, stg, ew, warp, lane, abort_flag,
-                                                  err_flag, tmO);
+                                                  err_flag, tmO, tmC);
   } else {
   const int quarter = warp & 3;              // TMEM lanes quarter*32 .. +31
   const int part = ew >> 2;                  // which share of the tile's columns
@@ -790,8 +810,8 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
 template <int MODE, int OP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmX, int M, int N, int K, Epilogue epi,
-               int* err_flag) {
+               const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+               int M, int N, int K, Epilogue epi, int* err_flag) {
   constexpr int EW = epi_warps(MODE);
   constexpr int BN = 256;
   using C = Cfg2<MODE>;
@@ -927,16 +947,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
                              release, stg, xbar0 + 8u * (ew * RES_BUFS), ew, warp, lane,
                              abort_flag, err_flag);
     } else {
-      const CUtensorMap* tmO = epi.tma_out ? &tmX : nullptr;
+      const CUtensorMap* tmO = (epi.tma_out & 1) ? &tmX : nullptr;
+      const CUtensorMap* tmC = (epi.tma_out & 2) ? &tmY : nullptr;
       for (int t = cid; t < total; t += ncl) {
         const int m0 = (t / num_n) * 2 * BM + (int)rank * BM, n_blk = t % num_n;
         if (!epilogue_tile<BN, MODE, EW, OP, true>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
                                              tfull_bar(acc), acc_phase, map_to_rank(tempty_bar(acc), 0),
-                                             release, stg, ew, warp, lane, abort_flag, err_flag, tmO))
+                                             release, stg, ew, warp, lane, abort_flag, err_flag, tmO,
+                                             tmC))
           break;
         if (++acc == 2) acc = 0, acc_phase ^= 1u;
       }
-      if (tmO && lane == 0) bulk_wait_group_all();   // TMA stores done before the CTA exits
+      if ((tmO || tmC) && lane == 0) bulk_wait_group_all();   // TMA stores done before exit
     }
   }
   tc_fence_before();
@@ -1006,7 +1028,7 @@ static cudaError_t launch_tc2(const void* A, const void* W, int M, int N, int K,
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = set_max_dynamic_smem((const void*)k_gemm_tc2<MODE, OP>, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  CUtensorMap ma, mb, mx;
+  CUtensorMap ma, mb, mx, my;
   if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, 128))
     return cudaErrorInvalidValue;
   Epilogue ek = epi;
@@ -1024,10 +1046,26 @@ static cudaError_t launch_tc2(const void* A, const void* W, int M, int N, int K,
   } else {
     mx = ma;   // unused
   }
+  my = ma;   // unused unless the K/V cache map below is made
+  // the store mode's out1 (the K/V cache: blocks of rpg rows, gstride rows per group) by TMA
+  // through a 3-D map when its blocks tile the cache exactly
+  if (MODE == EPI_STORE && epi.act_bf16 && epi.split < N && epi.out1 && epi.map1.rpg >= 32 &&
+      epi.map1.gstride % epi.map1.rpg == 0 && epi.map1.goff % epi.map1.rpg == 0 &&
+      (((uintptr_t)epi.out1) & 15) == 0 && (epi.ld1 % 8) == 0) {
+    const RowMap& m1 = epi.map1;
+    // an identity map (one block of at least M rows) is encoded as a single block of M rows
+    const int rpg_dim = m1.rpg >= M ? M : m1.rpg;
+    const long long nblocks =
+        (long long)((M - 1) / m1.rpg) * (m1.gstride / m1.rpg) + m1.goff / m1.rpg + 1;
+    if (make_map_bf16_blocks(&my, epi.out1, N - epi.split, rpg_dim, nblocks, epi.ld1))
+      ek.tma_out |= 2;   // else the rows leave by per-lane stores
+    else
+      my = ma;
+  }
   const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
   const int pairs = num_sms / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  k_gemm_tc2<MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, mx, M, N, K, ek, err_flag);
+  k_gemm_tc2<MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, mx, my, M, N, K, ek, err_flag);
   return cudaGetLastError();
 }
 
