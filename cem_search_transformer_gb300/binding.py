@@ -28,7 +28,8 @@ EXPORTS = ("jepa_create", "jepa_destroy", "jepa_last_error", "jepa_status_string
            "jepa_profile_read", "jepa_sync_check", "jepa_energy_l1_noalloc",
            "jepa_attention_bf16", "jepa_cem_warm_start", "jepa_world_model_step",
            "jepa_cem_closed_loop", "jepa_linear_fp8", "jepa_quantize_rows_fp8",
-           "jepa_set_use_graphs", "jepa_selftest_bounded_wait")
+           "jepa_set_use_graphs", "jepa_selftest_bounded_wait", "jepa_linear_resid_bf16",
+           "jepa_linear_qkv_bf16")
 
 
 class JepaError(RuntimeError):
@@ -78,6 +79,8 @@ def load(path: str = _LIB_PATH):
         "jepa_cem_plan": ([P, P, P, P, P, P, I, I, I, I, I, U64, P, ctypes.POINTER(Trace), P], I),
         "jepa_plan_kernel_count": ([P, I, I, I, I, I, ctypes.POINTER(ctypes.c_int64)], I),
         "jepa_linear_bf16": ([P, P, P, P, I, I, I, I, P, P], I),
+        "jepa_linear_resid_bf16": ([P, P, P, P, I, I, I, P, P], I),
+        "jepa_linear_qkv_bf16": ([P, P, P, P, I, I, I, I, I, I, P, P, P], I),
         "jepa_profile_enable": ([P, I], I),
         "jepa_profile_read": ([P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                ctypes.POINTER(ctypes.c_int64)], I),
@@ -338,6 +341,22 @@ class Planner:
             self.h, _arg(A, "A", "bf16", M * K), _arg(W, "W", "bf16", N * K),
             _arg(bias, "bias", "f32", N, optional=True), M, N, K, int(gelu),
             _arg(out, "out", "f32", M * n_out), _stream(stream)), "linear_bf16")
+
+    def linear_resid_bf16(self, A, W, bias, M, N, K, x, stream=None):
+        self._dims(M=M, N=N, K=K)
+        self._check(self.lib.jepa_linear_resid_bf16(
+            self.h, _arg(A, "A", "bf16", M * K), _arg(W, "W", "bf16", N * K),
+            _arg(bias, "bias", "f32", N, optional=True), M, N, K,
+            _arg(x, "x", "f32", M * N), _stream(stream)), "linear_resid_bf16")
+
+    def linear_qkv_bf16(self, A, W, bias, M, d, K, T, kv_rows, frame, q, kv, stream=None):
+        self._dims(M=M, d=d, K=K, T=T, kv_rows=kv_rows)
+        ncand = -(-int(M) // int(T))
+        self._check(self.lib.jepa_linear_qkv_bf16(
+            self.h, _arg(A, "A", "bf16", M * K), _arg(W, "W", "bf16", 3 * d * K),
+            _arg(bias, "bias", "f32", 3 * d, optional=True), M, d, K, T, kv_rows, int(frame),
+            _arg(q, "q", "bf16", M * d), _arg(kv, "kv", "bf16", ncand * kv_rows * 2 * d),
+            _stream(stream)), "linear_qkv_bf16")
 
     def linear_fp8(self, A, a_scale, W, w_scale, bias, M, N, K, gelu, out, stream=None):
         self._dims(M=M, N=N, K=K)

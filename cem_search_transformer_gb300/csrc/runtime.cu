@@ -1154,6 +1154,49 @@ jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W
   return JEPA_OK;
 }
 
+jepa_status jepa_linear_resid_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W,
+                                   const float* bias, int M, int N, int K, float* x,
+                                   void* stream) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  if (!bf16_mode(ctx)) return fail(ctx, JEPA_ERR_UNSUPPORTED, "linear_resid_bf16 needs a bf16 context");
+  if (bad_ptr(A) || bad_ptr(W) || bad_ptr(x) || M < 1 || N < 4 || N % 4 || K < 8 || K % 8)
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_resid_bf16: bad argument");
+  if ((((uintptr_t)A) & 15) || (((uintptr_t)W) & 15) || (((uintptr_t)x) & 15))
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_resid_bf16: A, W and x must be 16-byte aligned");
+  CK(cudaSetDevice(ctx->device));
+  Epilogue e = epi_base(ctx, EPI_RESID);
+  e.bias = bias;
+  e.out0 = x;
+  e.ld0 = N;
+  CK(gemm_tc_bf16((const bf16*)A, (const bf16*)W, M, N, K, e, ctx->dev_err, ctx->num_sms,
+                  (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
+jepa_status jepa_linear_qkv_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W,
+                                 const float* bias, int M, int d, int K, int T, int kv_rows,
+                                 int frame, uint16_t* q, uint16_t* kv, void* stream) {
+  if (!ctx) return JEPA_ERR_INVALID_ARG;
+  if (!bf16_mode(ctx)) return fail(ctx, JEPA_ERR_UNSUPPORTED, "linear_qkv_bf16 needs a bf16 context");
+  if (bad_ptr(A) || bad_ptr(W) || bad_ptr(q) || bad_ptr(kv) || M < 1 || d < 32 || d % 32 ||
+      K < 8 || K % 8 || T < 1 || frame < 0 || (long long)(frame + 1) * T > kv_rows)
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_qkv_bf16: bad argument");
+  if ((((uintptr_t)A) & 15) || (((uintptr_t)W) & 15))
+    return fail(ctx, JEPA_ERR_INVALID_ARG, "linear_qkv_bf16: A and W must be 16-byte aligned");
+  CK(cudaSetDevice(ctx->device));
+  Epilogue e = epi_base(ctx, EPI_STORE);
+  e.bias = bias;
+  e.out0 = q;
+  e.ld0 = d;
+  e.split = d;
+  e.out1 = kv;
+  e.ld1 = 2 * d;
+  e.map1 = RowMap{T, (long long)kv_rows, (long long)frame * T};
+  CK(gemm_tc_bf16((const bf16*)A, (const bf16*)W, M, 3 * d, K, e, ctx->dev_err, ctx->num_sms,
+                  (cudaStream_t)stream));
+  return JEPA_OK;
+}
+
 jepa_status jepa_linear_fp8(jepa_ctx* ctx, const uint8_t* A, const float* a_scale,
                             const uint8_t* W, const float* w_scale, const float* bias, int M,
                             int N, int K, int gelu, float* out, void* stream) {

@@ -233,6 +233,30 @@ jepa_status jepa_linear_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W
                              const float* bias, int M, int N, int K, int gelu, float* out,
                              void* stream);
 
+/* The residual GEMM of the predictor on caller data (the attention out-projection and the
+ * MLP down-projection of a pre-LN block, "Real-time inference for JEPA world-model
+ * architectures with Ray", the predictor of section "Measured on 8x A100"):
+ *   x[M,N] += A[M,K] * W[N,K]^T + bias[N], fp32 accumulation, x fp32 updated in place.
+ *   A, W: bf16 bit patterns dev, 16-byte aligned; bias [N] dev or NULL; x [M,N] fp32 dev.
+ *   K a multiple of 8, N a multiple of 4. Needs a bf16 context. */
+jepa_status jepa_linear_resid_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W,
+                                   const float* bias, int M, int N, int K, float* x,
+                                   void* stream);
+
+/* The QKV GEMM of the predictor on caller data, writing one rollout step's rows into the
+ * candidates' K/V caches (KV cache across rollout steps, the planning page, "Measured on
+ * 8x A100"): acc = A[M,K] * W[3d,K]^T + bias[3d] (fp32), rounded to bf16, and for each
+ * row r < M, with candidate c = r / T and t = r % T,
+ *   q[r, 0:d] = acc[r, 0:d],   kv[c][frame*T + t][0:2d] = acc[r, d:3d].
+ * Other rows of kv are not written.
+ *   A, W: bf16 bit patterns dev, 16-byte aligned; bias [3d] dev or NULL;
+ *   q [M, d] and kv [ceil(M/T)][kv_rows][2d]: bf16 bit patterns dev.
+ *   d a multiple of 32, K a multiple of 8, T >= 1, 0 <= frame, (frame + 1) * T <= kv_rows.
+ * Needs a bf16 context. */
+jepa_status jepa_linear_qkv_bf16(jepa_ctx* ctx, const uint16_t* A, const uint16_t* W,
+                                 const float* bias, int M, int d, int K, int T, int kv_rows,
+                                 int frame, uint16_t* q, uint16_t* kv, void* stream);
+
 /* The fp8 GEMM of the FP8 mode on caller data: out[M,N] = act((A[M,K] * W[N,K]^T) *
  * a_scale[M] (rows) * w_scale[N] (columns) + bias[N]), A and W e4m3 codes (one byte each,
  * OCP E4M3: bias 7, no infinities, largest 448), fp32 accumulation, fp32 output.

@@ -111,3 +111,64 @@ def test_gated_linear_rejects_bad_shapes(planner):
         planner.linear_bf16(A, W, bias, 64, 384, 64, 2, out)      # N not a multiple of 256
     with pytest.raises(JepaError):
         planner.linear_bf16(A, W[:256], None, 64, 256, 64, 2, out)  # gated needs a bias
+
+
+def _bf16_to_f64(bits):
+    """bf16 bit patterns (int16 / uint16 array) as float64 values."""
+    return (bits.astype(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("M,N,K", [(8000, 1024, 1024),   # CTA pairs: several tiles per pair,
+                                                          # both accumulators, ragged last tile
+                                   (4100, 768, 256),     # CTA pairs, M not a multiple of 32
+                                   (300, 384, 192)])     # single CTAs
+def test_linear_resid_matches_matmul(planner, M, N, K):
+    """Residual GEMM (attention out-projection / MLP down-projection): x += A W^T + b in fp32,
+    against the same sum in float64 on bf16-representable A and W."""
+    rng = np.random.default_rng(M + N + K + 1)
+    A = predictor.round_to_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    W = predictor.round_to_bf16((rng.standard_normal((N, K)) * 0.05).astype(np.float32))
+    bias = rng.standard_normal(N).astype(np.float32)
+    x0 = rng.standard_normal((M, N)).astype(np.float32)
+    x = cuda(x0)
+    planner.linear_resid_bf16(cuda(_bf16_bits(A).astype(np.int16)), cuda(_bf16_bits(W).astype(np.int16)),
+                              cuda(bias), M, N, K, x)
+    planner.sync_check()
+    ref = x0.astype(np.float64) + A.astype(np.float64) @ W.astype(np.float64).T + bias
+    scale = np.sqrt(K) * 0.05 + 1.0
+    assert np.max(np.abs(host(x) - ref)) < 2e-5 * scale * 10, np.max(np.abs(host(x) - ref))
+
+
+@pytest.mark.parametrize("ncand,T,d,K,frame,kv_frames,cut",
+                         [(9, 258, 256, 256, 1, 3, 0),     # CTA pairs; 32-row chunks straddle
+                                                           # candidates; a middle frame
+                          (9, 258, 256, 256, 2, 3, 100),   # last frame, last candidate partial
+                          (9, 66, 256, 128, 0, 2, 0),      # CTA pairs, blocks of 66 rows
+                          (3, 40, 64, 64, 1, 2, 0)])       # single CTAs (3d = 192)
+def test_linear_qkv_writes_cache_rows(planner, ncand, T, d, K, frame, kv_frames, cut):
+    """QKV GEMM with the K/V-cache epilogue: q rows and the frame's cache rows hold
+    bf16(A W^T + b) (within one bf16 rounding of the float64 sum), and no other cache row is
+    written."""
+    M = ncand * T - cut
+    kv_rows = kv_frames * T
+    rng = np.random.default_rng(M + d + K + frame)
+    A = predictor.round_to_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    W = predictor.round_to_bf16((rng.standard_normal((3 * d, K)) * 0.05).astype(np.float32))
+    bias = rng.standard_normal(3 * d).astype(np.float32)
+    q = torch.zeros(M, d, dtype=torch.int16, device="cuda")
+    kv = torch.zeros(ncand, kv_rows, 2 * d, dtype=torch.int16, device="cuda")
+    planner.linear_qkv_bf16(cuda(_bf16_bits(A).astype(np.int16)), cuda(_bf16_bits(W).astype(np.int16)),
+                            cuda(bias), M, d, K, T, kv_rows, frame, q, kv)
+    planner.sync_check()
+    ref = A.astype(np.float64) @ W.astype(np.float64).T + bias
+    tol = 2.0 ** -7 * np.abs(ref) + 1e-4      # one bf16 rounding (2^-8 relative) plus slack
+    got_q = _bf16_to_f64(host(q))
+    assert np.all(np.abs(got_q - ref[:, :d]) <= tol[:, :d])
+    kvh = host(kv)
+    got_kv = _bf16_to_f64(kvh)
+    rows = np.arange(M)
+    c, t = rows // T, rows % T
+    assert np.all(np.abs(got_kv[c, frame * T + t] - ref[:, d:]) <= tol[:, d:])
+    written = np.zeros((ncand, kv_rows), bool)
+    written[c, frame * T + t] = True
+    assert not np.any(kvh[~written]), "cache rows outside the frame's rows were written"
