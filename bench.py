@@ -45,9 +45,9 @@ METRIC = "CEM plan-step latency (ms, 800x10) and candidate rollouts/sec, % of ro
 # GEMM_TRAFFIC_SOURCE_SHA (first 16 hex digits of the SHA-256 of gemm_tc.cu, tc_common.cuh
 # and common.cuh, in that order); when the kernels change, the line reports no traffic until
 # the counters are taken again.
-GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (433.0e6 + 1193.3e6, 1272.1e6 + 761.2e6, 437.6e6 + 1613.3e6,
-                                   2677.2e6 + 816.8e6)
-GEMM_TRAFFIC_SOURCE_SHA = "920534fdc0d7fad1"
+GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (432.9e6 + 1195.3e6, 1274.0e6 + 757.2e6, 437.7e6 + 1615.8e6,
+                                   2705.9e6 + 802.7e6)
+GEMM_TRAFFIC_SOURCE_SHA = "f2f4923596139b72"
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
