@@ -10,12 +10,18 @@
 //   - warps 2..: epilogue, EW warps in all (8, or 16 for the GELU and gated layers whose
 //     erf is the expensive part), EW/4 warps per TMEM lane quarter, each taking a 4/EW
 //     share of the tile's columns. A warp reads 32 rows x 32 columns with tcgen05.ld
-//     32x32b.x32 (thread = row). The GELU and gated epilogues apply bias and activation in
-//     that layout and stage only bf16 results; the others transpose fp32 accumulators
-//     through a swizzled 4 KB shared-memory buffer so that each global access covers
-//     contiguous columns of a row, and apply bias / residual / position / L1 energy (see
-//     common.cuh) four columns at a time. The next chunk's TMEM load is in flight while the
-//     current chunk is processed.
+//     32x32b.x32 (thread = row) and releases the accumulator with a relaxed arrive once its
+//     last TMEM load has landed. The GELU and gated epilogues (and, on CTA pairs, the QKV
+//     store) apply bias and activation in that layout and stage only bf16 results, in the
+//     64-byte swizzle of a 32 x 32 TMA box: on CTA pairs a TMA store writes each chunk
+//     (K/V cache rows through a 3-D map of the cache's per-candidate blocks). The residual
+//     epilogue of CTA pairs loads each 32 x 32 chunk of x by TMA into a 128-byte-swizzled
+//     buffer, adds accumulator and bias per lane in place and stores it back by TMA. The
+//     single-CTA kernel's other epilogues transpose fp32 accumulators through a swizzled
+//     4 KB shared-memory buffer so that each global access covers contiguous columns of a
+//     row, and apply bias / residual / position / L1 energy (see common.cuh) four columns
+//     at a time. The next chunk's TMEM load is in flight while the current chunk is
+//     processed.
 //   - two TMEM accumulators (2 x BN columns) so the epilogue of tile i overlaps the MMAs of
 //     tile i+1;
 //   - QKV, the MLP up-projection and the residual projections run on CTA pairs
