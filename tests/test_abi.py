@@ -92,3 +92,41 @@ def test_binding_refuses_host_tensors_for_device_arguments():
     assert binding._arg(None, "goal", "f32", 1, optional=True) is None
     assert binding._arg(1234, "goal", "f32", 1 << 40) == 1234       # raw address: caller's word
     assert binding._arg(g, "goal", "f32", B * P * E, host_ok=True) == g.data_ptr()
+
+
+def test_kernel_entry_points_check_arguments_before_the_call():
+    """The residual and QKV-cache GEMM wrappers reject bad sizes and host tensors before the
+    library is called (a stand-in object without a library or context takes the Planner's
+    place, so a call that got past the checks would fail differently)."""
+    import torch
+    from cem_search_transformer_gb300 import binding
+
+    class Unreachable:
+        def __getattr__(self, name):
+            def call(*args):
+                raise AssertionError(f"{name} was called although an argument was invalid")
+            return call
+
+    class NoLibrary:
+        lib = Unreachable()
+        h = None
+        _dims = binding.Planner._dims
+
+        def _check(self, status, what):
+            raise AssertionError(f"{what} returned {status} although an argument was invalid")
+
+    M, N, K, d, T = 64, 128, 64, 64, 16
+    A = torch.zeros(M, K, dtype=torch.int16)
+    W = torch.zeros(N, K, dtype=torch.int16)
+    x = torch.zeros(M, N)
+    with pytest.raises(binding.JepaError, match="CUDA"):
+        binding.Planner.linear_resid_bf16(NoLibrary(), A, W, None, M, N, K, x)
+    with pytest.raises(binding.JepaError, match=">= 1"):
+        binding.Planner.linear_resid_bf16(NoLibrary(), A, W, None, 0, N, K, x)
+    Wq = torch.zeros(3 * d, K, dtype=torch.int16)
+    q = torch.zeros(M, d, dtype=torch.int16)
+    kv = torch.zeros(M // T, 2 * T, 2 * d, dtype=torch.int16)
+    with pytest.raises(binding.JepaError, match="CUDA"):
+        binding.Planner.linear_qkv_bf16(NoLibrary(), A, Wq, None, M, d, K, T, 2 * T, 1, q, kv)
+    with pytest.raises(binding.JepaError, match=">= 1"):
+        binding.Planner.linear_qkv_bf16(NoLibrary(), A, Wq, None, M, d, K, 0, 2 * T, 1, q, kv)
