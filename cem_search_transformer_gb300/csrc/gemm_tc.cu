@@ -58,19 +58,23 @@ __host__ __device__ constexpr int stg_floats(int mode) {
 template <int BN, int MODE>
 struct Cfg {
   static constexpr int EW = epi_warps(MODE);
-  static constexpr int STG = stg_floats(MODE);
+  // the projection to E stages goal chunks (two 32 x 32 fp32 TMA boxes per warp) in the
+  // transpose buffer's place when it computes energies only
+  static constexpr int STG = MODE == EPI_OUTPROJ ? 2 * STG_FLOATS : stg_floats(MODE);
+  static constexpr int XBARS = MODE == EPI_OUTPROJ ? 2 * EW : 0;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // as many ring stages (up to 6) as the shared memory left by the staging buffers holds
-  static constexpr int FIT = (232448 - 1024 - 16 - 5 * 8 - EW * STG * 4) / (STAGE_BYTES + 16);
+  static constexpr int FIT =
+      (232448 - 1024 - 16 - (5 + XBARS) * 8 - EW * STG * 4) / (STAGE_BYTES + 16);
   static constexpr int STAGES = FIT < 6 ? FIT : 6;
   static constexpr int TMEM_COLS = 2 * BN;   // two accumulators; 256 or 512 (power of 2)
   // ring, epilogue transpose buffers, barriers (full/empty per stage, tfull/tempty per
   // accumulator, teardown), TMEM address slot + abort flag, 1024 B alignment slack
   static constexpr int STG_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + EW * STG * 4;
-  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5) * 8 + 16 + 1024;
+  static constexpr int SMEM = BAR_OFF + (2 * STAGES + 5 + XBARS) * 8 + 16 + 1024;
   static_assert(STAGES >= 3 && SMEM <= 232448, "shared memory budget");
 };
 
@@ -533,6 +537,125 @@ __device__ __forceinline__ bool epilogue_tile(const Epilogue& epi, int M, int N,
   }
 }
 
+// Energy-only epilogue of the projection to E (EPI_OUTPROJ with a goal and no z outputs) in
+// the single-CTA kernel, run by each epilogue warp over all of its tiles. Per 32 x 32 chunk
+// the goal rows of the chunk's candidate (32 consecutive goal rows, as P is a multiple of
+// 32) arrive by TMA in one of two 128-byte-swizzled buffers, loaded two chunks ahead across
+// tile boundaries; each lane takes its accumulator row from TMEM (thread = row), forms
+// z = acc (* scales) + bias and sums |z - goal| over the warp's columns of the tile in
+// column order, and writes that sum as the row's partial for the tile and column share.
+// Reading the goal per element through L1 limited the projection (883 us per full-size
+// launch, 629 without the goal reads).
+template <int BN, int EW, int OP, typename Release>
+__device__ __forceinline__ bool epilogue_energy_tma(const CUtensorMap* tmG, const Epilogue& epi,
+                                                    int M, int N, int num_n, int total,
+                                                    uint32_t tmem_base, const uint32_t (&tfull)[2],
+                                                    const uint32_t (&tempty)[2], Release release,
+                                                    float* bufs, uint32_t gbar0, int ew, int warp,
+                                                    int lane, volatile int* abort_flag,
+                                                    int* err_flag) {
+  constexpr int SPAN = BN * 4 / EW;          // columns per epilogue warp and tile
+  constexpr int NCH = SPAN / 32;             // 32-column chunks per tile
+  constexpr int NB = 2;                      // goal buffers per warp
+  const int quarter = warp & 3, part = ew >> 2;
+  const int bid = blockIdx.x, nblk = gridDim.x;
+  const int my_tiles = bid < total ? (total - 1 - bid) / nblk + 1 : 0;
+  const int nchunks = my_tiles * NCH;
+  const uint32_t buf0 = smem_u32(bufs);
+  auto chunk_rc = [&](int g, int& row_base, int& c0) {
+    const int t = bid + (g / NCH) * nblk;
+    row_base = (t / num_n) * BM + quarter * 32;
+    c0 = (t % num_n) * BN + part * SPAN + 32 * (g % NCH);
+  };
+  auto issue_goal = [&](int g) {   // lane 0 only
+    if (g >= nchunks) return;
+    const uint32_t bar = gbar0 + 8u * (g % NB);
+    int row_base, c0;
+    chunk_rc(g, row_base, c0);
+    if (row_base < M && c0 < N) {
+      const int cand = epi.cand0 + row_base / epi.P;
+      const int grow = (cand / epi.cands_per_problem) * epi.P + row_base % epi.P;
+      mbar_expect_tx(bar, STG_FLOATS * 4);
+      tma_load_2d(buf0 + (g % NB) * STG_FLOATS * 4, tmG, c0, grow, bar);
+    } else {
+      mbar_arrive(bar);   // nothing of this chunk is used
+    }
+  };
+  if (lane == 0)
+    for (int g = 0; g < NB; ++g) issue_goal(g);
+  bool ok = true;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  for (int i = 0; i < my_tiles && ok; ++i) {
+    const int t = bid + i * nblk;
+    const int row = (t / num_n) * BM + quarter * 32 + lane;
+    const int n_blk = t % num_n;
+    const uint32_t tbase =
+        tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(part * SPAN);
+    if (!mbar_wait(tfull[acc], acc_phase, abort_flag, err_flag)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    float rs = 1.f;                          // fp8: this lane's row scale
+    if constexpr (OP) rs = row < M ? epi.row_scale[row] : 0.f;
+    uint32_t r[32];
+    tmem_ld32_async(tbase, r);
+    float esum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int g = i * NCH + j;
+      tmem_wait(r);
+      if (j == NCH - 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release(tempty[acc]);
+      }
+      if (!mbar_wait(gbar0 + 8u * (g % NB), (uint32_t)(g / NB) & 1u, abort_flag, err_flag)) {
+        ok = false;
+        break;
+      }
+      int row_base, c0;
+      chunk_rc(g, row_base, c0);
+      // row `lane` of the goal box: 16-byte piece k at k ^ (lane & 7) (128-byte swizzle)
+      const float* grow_s = bufs + (g % NB) * STG_FLOATS + lane * 32;
+      float4 gv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) gv[k] = *reinterpret_cast<const float4*>(grow_s + ((k ^ (lane & 7)) << 2));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) issue_goal(g + NB);     // the buffer has been read by every lane
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = c0 + 4 * k;
+        if (c >= N) break;
+        float4 v = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                               __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+        if constexpr (OP) {
+          const float4 cs = __ldg(reinterpret_cast<const float4*>(epi.col_scale + c));
+          v.x *= rs * cs.x; v.y *= rs * cs.y; v.z *= rs * cs.z; v.w *= rs * cs.w;
+        }
+        const float4 bb = epi_bias4(epi, c);
+        v.x += bb.x; v.y += bb.y; v.z += bb.z; v.w += bb.w;
+        esum += ((fabsf(v.x - gv[k].x) + fabsf(v.y - gv[k].y)) + fabsf(v.z - gv[k].z)) +
+                fabsf(v.w - gv[k].w);
+      }
+      if (j + 1 < NCH) tmem_ld32_async(tbase + 32u * (j + 1), r);   // r is free again
+    }
+    if (!ok) break;
+    if (row < M) epi.partial[(long long)row * epi.ntiles + (EW / 4) * n_blk + part] = esum;
+    if (++acc == 2) acc = 0, acc_phase ^= 1u;
+  }
+  if (!ok && lane == 0) {
+    // goal loads may still be in flight into this CTA's shared memory: let them land
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 2000000ull) {
+    }
+  }
+  __syncwarp();
+  return ok;
+}
+
 // Residual epilogue of the CTA-pair kernel (EPI_RESID: x[r, c] += acc + bias; x fp32 with
 // the identity row map and row stride N), run by each epilogue warp over all of its tiles.
 // Global loads through L1 limit the bytes a warp can keep in flight, and x is read and
@@ -656,7 +779,8 @@ __device__ __forceinline__ bool epilogue_resid_tma(const CUtensorMap* tmX, const
 template <int BN, int MODE, int OP>
 __global__ void __launch_bounds__(cta_threads(MODE), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              int M, int N, int K, Epilogue epi, int* err_flag) {
+              const __grid_constant__ CUtensorMap tmX, int M, int N, int K, Epilogue epi,
+              int* err_flag) {
   constexpr int EW = epi_warps(MODE);
   using C = Cfg<BN, MODE>;
   extern __shared__ uint8_t smem_raw[];
@@ -668,7 +792,8 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
   const uint32_t teardown_bar = bar0 + 8u * (2 * C::STAGES + 4);
-  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + (2 * C::STAGES + 5) * 8);
+  const uint32_t xbar0 = bar0 + 8u * (2 * C::STAGES + 5);   // goal buffers (EPI_OUTPROJ)
+  uint32_t* tmem_slot = (uint32_t*)(smem + C::BAR_OFF + (2 * C::STAGES + 5 + C::XBARS) * 8);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -688,6 +813,7 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
       mbar_init(tempty_bar(a), EW);   // one arrival per epilogue warp
     }
     mbar_init(teardown_bar, 1);
+    for (int b = 0; b < C::XBARS; ++b) mbar_init(xbar0 + 8u * b, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -790,7 +916,18 @@ __global__ void __launch_bounds__(cta_threads(MODE), 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     auto release = [](uint32_t bar) { mbar_arrive_relaxed(bar); };
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    bool streamed = false;   // all tiles done by the energy epilogue
+    if constexpr (MODE == EPI_OUTPROJ) {
+      if (epi.tma_out & 4) {
+        const uint32_t tf[2] = {tfull_bar(0), tfull_bar(1)};
+        const uint32_t te[2] = {tempty_bar(0), tempty_bar(1)};
+        epilogue_energy_tma<BN, EW, OP>(&tmX, epi, M, N, num_n, total, tmem_base, tf, te, release,
+                                        stg, xbar0 + 8u * (ew * 2), ew, warp, lane, abort_flag,
+                                        err_flag);
+        streamed = true;
+      }
+    }
+    for (int t = blockIdx.x; t < total && !streamed; t += gridDim.x) {
       const int m0 = (t / num_n) * BM, n_blk = t % num_n;
       if (!epilogue_tile<BN, MODE, EW, OP, false>(epi, M, N, m0, n_blk, tmem_base + (uint32_t)(acc * BN),
                                        tfull_bar(acc), acc_phase, tempty_bar(acc), release, stg, ew,
@@ -996,12 +1133,22 @@ static cudaError_t launch_tc(const void* A, const void* W, int M, int N, int K, 
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = set_max_dynamic_smem((const void*)k_gemm_tc<BN, MODE, OP>, C::SMEM, attr_done);
   if (e != cudaSuccess) return e;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mx;
   if (!operand_map<OP>(&ma, A, M, K, BM) || !operand_map<OP>(&mb, W, N, K, BN))
     return cudaErrorInvalidValue;
+  Epilogue ek = epi;
+  ek.tma_out = 0;
+  mx = ma;   // unused unless the goal map below is made
+  // energies only: the goal rows arrive by TMA (32-row chunks stay within one candidate)
+  if (MODE == EPI_OUTPROJ && epi.goal && !epi.zpred && !epi.zhat && epi.P % 32 == 0 &&
+      (((uintptr_t)epi.goal) & 15) == 0) {
+    const int problems = (epi.cand0 + (M - 1) / epi.P) / epi.cands_per_problem + 1;
+    if (make_map_f32(&mx, epi.goal, problems * epi.P, N, 32)) ek.tma_out = 4;
+    else mx = ma;
+  }
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms ? tiles : num_sms;
-  k_gemm_tc<BN, MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, M, N, K, epi, err_flag);
+  k_gemm_tc<BN, MODE, OP><<<grid, cta_threads(MODE), C::SMEM, s>>>(ma, mb, mx, M, N, K, ek, err_flag);
   return cudaGetLastError();
 }
 
