@@ -47,7 +47,7 @@ METRIC = "CEM plan-step latency (ms, 800x10) and candidate rollouts/sec, % of ro
 # the counters are taken again.
 GEMM_DRAM_BYTES_PER_LAUNCH_FULL = (432.9e6 + 1195.3e6, 1274.0e6 + 757.2e6, 437.7e6 + 1615.8e6,
                                    2705.9e6 + 802.7e6)
-GEMM_TRAFFIC_SOURCE_SHA = "f7a29269e6c8387e"
+GEMM_TRAFFIC_SOURCE_SHA = "f46d6499d7959abf"
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -78,8 +78,10 @@ struct Epilogue {
   // (activation row scale, weight output-channel scale) before the bias
   const float* row_scale;
   const float* col_scale;
-  // set by the CTA-pair launcher only: 1 when bf16 out0 (identity rows) leaves the GELU and
-  // gated epilogues by TMA stores through the kernel's output tensor map
+  // set by the GEMM launchers only (callers leave it 0): which epilogue data move by TMA
+  // through the kernel's extra tensor maps. CTA pairs: bit 0 = bf16 out0 rows (identity row
+  // map) by TMA stores, bit 1 = out1 K/V cache rows by TMA stores (3-D map of row blocks).
+  // Single CTAs: bit 2 = the projection's goal rows by TMA loads (energies only).
   int tma_out;
 };
 
