@@ -72,3 +72,12 @@ def test_fp8_step_roofline_counts_e4m3_products_at_twice_the_rate():
     att = bench.attention_flops(pc, 1)
     r = bench.step_roofline(pc, 1, 1, None, 1.0, peaks)
     assert r["ms_at_measured_burst"] == pytest.approx((f8 / 4000e12 + (f16 + att) / 2000e12) * 1e3)
+
+
+def test_committed_gemm_traffic_belongs_to_the_committed_kernels():
+    """The DRAM traffic bench.py reports for the GEMMs was counted on the kernels whose
+    source it names; an edit of that source without new counters (or without a statement
+    that the counted kernels are unchanged) makes the bench line report no traffic."""
+    assert bench.gemm_source_sha() == bench.GEMM_TRAFFIC_SOURCE_SHA
+    assert len(bench.GEMM_DRAM_BYTES_PER_LAUNCH_FULL) == 4
+    assert all(1e9 < b < 4e9 for b in bench.GEMM_DRAM_BYTES_PER_LAUNCH_FULL)
